@@ -1,0 +1,424 @@
+"""Benchmark of the MoE dispatch/combine hot path on GB300.
+
+One step = one pass of the whole path over the workload resident in HBM:
+layout -> notify -> dispatch -> combine (identity experts: combine reads the
+dispatch arena), all through the C ABI of libmoe.so on one stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. ``value`` is tokens/s over all ranks (S tokens per step
+per rank); the device-timed kernels give the roofline of the dominant kernel
+against the measured HBM copy bandwidth. ``--impl reference`` times the CPU
+oracle on a bounded sample of the same workload instead (host cores only).
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the path's P ranks are partitions of one GPU's memory) and the time is the
+maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of ~8 TB/s) on 1 GB300"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = ("combine_moe_layout_02_gb300/csrc/dispatch.cu", "combine_moe_layout_02_gb300/csrc/combine.cu",
+                  "combine_moe_layout_02_gb300/csrc/moe_device.cuh")
+
+
+# --------------------------------------------------------------------------
+# Algorithmic (minimum) bytes per launch.
+
+def dispatch_bytes(S, P, K, H, R, quant):
+    """Read x once, write each received row's payload + metadata, side arrays,
+    read topk ids/weights and the send_head row of every token."""
+    payload = H if quant else 2 * H
+    meta = 16 if quant else 12          # (scale +) triple
+    return 2 * S * H + R * (payload + meta) + R * 4 + R * K * 8 + S * K * 8 + S * P * 4
+
+
+def combine_bytes(S, P, K, H, R):
+    """Read every received row once, write out, read send_head and topk."""
+    return R * 2 * H + S * 2 * H + S * P * 4 + S * K * 8
+
+
+# --------------------------------------------------------------------------
+# Multi-rank helpers (also exercised on CPU with gloo).
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_s: float, units: float, world: int):
+    """Max of the ranks' times and sum of their units (no-op for one rank)."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# Clocks during the timed region.
+
+class ClockSampler:
+    def __init__(self, uuid: str | None, period_ms: int = 50):
+        self.uuid = uuid
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms={self.period_ms}"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 10 and f[2].replace(".", "").isdigit():
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        sm = [float(r[2]) for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][3]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the kernels as they are now."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("per_launch_bytes", {}).get(workload, {}).get(kernel)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle on a bounded sample (reference arm and cpu_baseline).
+
+def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int = 1000,
+                  workload=None):
+    """Time the oracle's full path on a bounded sample of the workload: the same
+    shape with T_sample tokens per rank. Returns tokens/s, passes, seconds and
+    a description of the sample."""
+    import oracle
+    from combine_moe_layout_02_gb300 import inputs
+
+    w = workload if workload is not None else inputs.workload(name, T=T_sample)
+    passes, t_total = 0, 0.0
+    while passes < max_passes and (passes == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        lay = oracle.layout(w.P, w.E, w.topk_idx)
+        nt = oracle.notify(w.P, w.E, w.C, w.expert_alignment, lay["num_tokens_per_rank"],
+                           lay["num_tokens_per_expert"], lay["is_token_in_rank"])
+        rows = int(nt["part_row_base"][-1])
+        dis = oracle.dispatch(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
+                              nt["send_head"], nt["part_row_base"], rows)
+        oracle.combine(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0), nt["part_row_base"],
+                       rows, nt["send_head"], w.topk_idx, w.topk_weights)
+        t_total += time.perf_counter() - t0
+        passes += 1
+    sample = (f"{name} with T={w.T} tokens per rank (S={w.S}, {passes} pass(es)); "
+              "single-threaded oracle: layout+notify+dispatch+combine")
+    return w.S * passes / t_total, passes, t_total, sample
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from combine_moe_layout_02_gb300 import inputs
+
+    w = inputs.workload(args.workload, T=args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _, _, _, sample = oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w)
+    elapsed = time.perf_counter() - t0
+    value = w.S * args.steps / elapsed
+    sample = sample.replace("1 pass(es)", f"{args.steps} timed steps of 1 pass")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(args.workload),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name):
+    from combine_moe_layout_02_gb300 import inputs
+
+    c = dict(inputs.WORKLOADS[name])
+    return {"workload": name, "P": c["P"], "E": c["E"], "S": c["P"] * c["T"], "H": c["H"],
+            "K": c["K"], "routing": c["routing"], "quant": c["quant"],
+            "num_channels": inputs.NUM_CHANNELS,
+            "l2": "no flush: inputs (x, receive arena) are larger than the 129 MB L2"}
+
+
+# --------------------------------------------------------------------------
+# Our arm.
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from combine_moe_layout_02_gb300 import inputs, moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = inputs.workload(args.workload)
+    shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, w.quant)
+    buf = moe.Buffers(shape, dev, side_arrays=True)
+    x_host = torch.from_numpy(w.x_bits.view(np.int16)).pin_memory()
+    idx_host = torch.from_numpy(w.topk_idx).pin_memory()
+    wts_host = torch.from_numpy(w.topk_weights).pin_memory()
+    x = x_host.to(dev)
+    idx = idx_host.to(dev)
+    wts = wts_host.to(dev)
+    out = torch.empty((w.S, w.H), dtype=torch.int16, device=dev)
+    out_host = torch.empty((w.S, w.H), dtype=torch.int16).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is None:
+            buf.step(x, idx, wts, out, stream)
+            return
+        ev[0].record(stream)
+        buf.layout(idx, stream)
+        buf.notify(stream)
+        ev[1].record(stream)
+        buf.dispatch(x, idx, wts, stream)
+        ev[2].record(stream)
+        buf.combine(out, idx, wts, stream=stream)
+        ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(buf.err[0].item()) != 0:
+        raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")
+    R = int(buf.part_row_base[-1].item())
+
+    # --- device-timed region: whole steps --------------------------------
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    elapsed_s = start.elapsed_time(end) / 1e3
+    clk = clocks.summary()
+    max_s, units = aggregate(elapsed_s, float(w.S * args.steps), world)
+    value = units / max_s
+
+    # --- per-kernel timing (same stream, events between the calls) --------
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize(dev)
+    t_front = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_disp = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_comb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    peak, peak_kind = measured_peaks()
+    db = dispatch_bytes(w.S, w.P, w.K, w.H, R, w.quant)
+    cb = combine_bytes(w.S, w.P, w.K, w.H, R)
+    disp_gbs = db / t_disp / 1e9
+    comb_gbs = cb / t_comb / 1e9
+    dominant = "dispatch" if t_disp >= t_comb else "combine"
+    ach = disp_gbs if dominant == "dispatch" else comb_gbs
+    kname = (("dispatch_int8_kernel" if w.quant else "dispatch_bf16_kernel") if dominant == "dispatch"
+             else "combine_kernel")
+
+    # --- end to end through the public API with host buffers -------------
+    h2d = x_host.numel() * 2 + idx_host.numel() * 4 + wts_host.numel() * 4
+    d2h = out_host.numel() * 2
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        idx.copy_(idx_host, non_blocking=True)
+        wts.copy_(wts_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_max, e_units = aggregate(e_start.elapsed_time(e_end) / 1e3, float(w.S * e2e_steps), world)
+    if int(buf.err[0].item()) != 0:
+        raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, passes, secs, sample = oracle_sample(args.workload, args.ref_tokens, args.cpu_seconds)
+        cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(args.workload),
+        "gpu_launches": 6 * args.steps,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
+                     "traffic": recorded_traffic(args.workload, kname),
+                     "algorithmic_bytes": db if dominant == "dispatch" else cb},
+        "stages": {
+            "layout_notify_us": 1e6 * t_front,
+            "dispatch": {"us": 1e6 * t_disp, "GB_s": disp_gbs, "frac_of_peak": disp_gbs / peak,
+                         "frac_of_8TBs": disp_gbs / 8000.0, "tokens_per_s": w.S / t_disp,
+                         "bytes": db},
+            "combine": {"us": 1e6 * t_comb, "GB_s": comb_gbs, "frac_of_peak": comb_gbs / peak,
+                        "frac_of_8TBs": comb_gbs / 8000.0, "tokens_per_s": w.S / t_comb,
+                        "bytes": cb},
+            "recv_rows": R,
+        },
+        "clocks": clk,
+        "e2e": {"value": e_units / e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    from combine_moe_layout_02_gb300 import inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens per rank of the oracle's bounded sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, 1 if world > 1 else world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1 and args.impl != "reference":
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+// api.cu -- the C ABI of libmoe.so (declared in include/moe.h): host-side
+// validation, scratch sizing and the launches on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+#include "moe_device.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Required array: non-NULL (unless it would hold no element) and aligned.
+bool ok_ptr(const void* p, int64_t elements, uintptr_t align) {
+    if (elements == 0) return p == nullptr || aligned(p, align);
+    return p != nullptr && aligned(p, align);
+}
+
+// Optional array: NULL, or aligned.
+bool ok_opt(const void* p, uintptr_t align) { return p == nullptr || aligned(p, align); }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int32_t status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_TOPK_OUT_OF_RANGE: return "MOE_ERR_TOPK_OUT_OF_RANGE";
+        case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+        case MOE_ERR_INCONSISTENT: return "MOE_ERR_INCONSISTENT";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+moe_status moe_check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->P < 1 || s->E < 1 || s->S < 0 || s->K < 1 || s->H < 1) return MOE_ERR_INVALID_ARG;
+    if (s->num_channels < 1 || s->expert_alignment < 1) return MOE_ERR_INVALID_ARG;
+    if (s->quant != 0 && s->quant != 1) return MOE_ERR_INVALID_ARG;
+    if (s->E % s->P != 0 || s->S % s->P != 0) return MOE_ERR_INVALID_ARG;
+    if (s->P > MOE_MAX_RANKS || s->E > MOE_MAX_EXPERTS || s->K > MOE_MAX_TOPK || s->H > MOE_MAX_HIDDEN)
+        return MOE_ERR_UNSUPPORTED;
+    if (s->num_channels > 4096) return MOE_ERR_UNSUPPORTED;
+    if (s->H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (s->quant && s->H % 16 != 0) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+int64_t moe_slot_stride(int32_t H, int32_t quant) {
+    if (H < 1) return -1;
+    const int64_t elt = quant ? 1 : 2;
+    return round_up(round_up(static_cast<int64_t>(H) * elt, 32) + 44, 512);
+}
+
+int64_t moe_scratch_bytes(const moe_shape* s) {
+    if (moe_check_shape(s) != MOE_OK) return -1;
+    const int64_t a = layout_plan(*s).scratch_bytes;
+    const int64_t b = notify_scratch_bytes(*s);
+    const int64_t m = a > b ? a : b;
+    return m > 256 ? m : 256;
+}
+
+int64_t moe_max_recv_rows(const moe_shape* s) {
+    if (moe_check_shape(s) != MOE_OK) return -1;
+    const int64_t m = s->K < s->P ? s->K : s->P;
+    return static_cast<int64_t>(s->S) * m;
+}
+
+moe_status moe_layout(const moe_shape* shape, const int32_t* topk_idx, int32_t* num_tokens_per_rank,
+                      int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                      uint32_t* is_token_in_rank_bits, int32_t* err, void* scratch,
+                      int64_t scratch_bytes, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (!ok_ptr(topk_idx, S * s.K, 16) || !ok_ptr(num_tokens_per_rank, 1, 16) ||
+        !ok_ptr(num_tokens_per_expert, 1, 16) || !ok_ptr(is_token_in_rank, S * s.P, 16) ||
+        !ok_opt(is_token_in_rank_bits, 16) || !ok_opt(err, 4) || !ok_ptr(scratch, 1, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_scratch_bytes(shape)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_layout(s, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                                   is_token_in_rank, is_token_in_rank_bits, err, scratch,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_notify(const moe_shape* shape, const int32_t* num_tokens_per_rank,
+                      const int32_t* num_tokens_per_expert, const uint8_t* is_token_in_rank,
+                      int32_t* rank_prefix_matrix, int32_t* channel_prefix_matrix,
+                      int32_t* recv_channel_prefix_matrix, int32_t* num_recv_tokens,
+                      int32_t* num_recv_tokens_per_expert, int32_t* recv_expert_offset,
+                      int32_t* send_head, int64_t* part_row_base, void* scratch,
+                      int64_t scratch_bytes, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (!ok_ptr(num_tokens_per_rank, 1, 16) || !ok_ptr(num_tokens_per_expert, 1, 16) ||
+        !ok_ptr(is_token_in_rank, S * s.P, 16) || !ok_ptr(rank_prefix_matrix, 1, 16) ||
+        !ok_ptr(channel_prefix_matrix, 1, 16) || !ok_ptr(recv_channel_prefix_matrix, 1, 16) ||
+        !ok_ptr(num_recv_tokens, 1, 16) || !ok_ptr(num_recv_tokens_per_expert, 1, 16) ||
+        !ok_ptr(recv_expert_offset, 1, 16) || !ok_ptr(send_head, S * s.P, 16) ||
+        !ok_ptr(part_row_base, 1, 16) || !ok_ptr(scratch, 1, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_scratch_bytes(shape)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_notify(s, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                                   rank_prefix_matrix, channel_prefix_matrix,
+                                   recv_channel_prefix_matrix, num_recv_tokens,
+                                   num_recv_tokens_per_expert, recv_expert_offset, send_head,
+                                   part_row_base, scratch, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                        const float* topk_weights, const int32_t* send_head,
+                        const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,
+                        int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                        int32_t* err, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (arena_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(x, S * s.H, 16) || !ok_ptr(topk_idx, S * s.K, 16) || !ok_ptr(send_head, S * s.P, 16) ||
+        !ok_ptr(part_row_base, 1, 16) || !ok_ptr(recv_arena, arena_rows, 16) ||
+        !ok_opt(recv_src_idx, 16) || !ok_opt(recv_topk_idx, 16) || !ok_opt(recv_topk_weights, 16) ||
+        !ok_opt(topk_weights, 16) || !ok_opt(err, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (recv_topk_weights && !topk_weights && S > 0) return MOE_ERR_INVALID_ARG;
+    DispatchArgs a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.K = s.K;
+    a.H = s.H;
+    a.epr = s.E / s.P;
+    a.S = S;
+    a.T = S / s.P;
+    a.x = x;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.send_head = send_head;
+    a.part_row_base = part_row_base;
+    a.arena = static_cast<uint8_t*>(recv_arena);
+    a.arena_rows = arena_rows;
+    a.stride = moe_slot_stride(s.H, s.quant);
+    a.scale_off = round_up(static_cast<int64_t>(s.H) * (s.quant ? 1 : 2), 32);
+    a.triple_off = a.scale_off + 32;
+    a.recv_src_idx = recv_src_idx;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_weights = recv_topk_weights;
+    a.err = err;
+    a.row_bytes = static_cast<uint32_t>(s.H) * 2u;
+    return from_cuda(launch_dispatch(s, a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stride,
+                       const int64_t* part_row_base, int64_t arena_rows, const int32_t* send_head,
+                       const int32_t* topk_idx, const float* topk_weights, uint16_t* out, int32_t* err,
+                       void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (arena_rows < 0 || y_row_stride < 2 * static_cast<int64_t>(s.H) || y_row_stride % 16 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(y, arena_rows, 16) || !ok_ptr(part_row_base, 1, 16) || !ok_ptr(send_head, S * s.P, 16) ||
+        !ok_ptr(topk_idx, S * s.K, 16) || !ok_opt(topk_weights, 16) || !ok_ptr(out, S * s.H, 16) ||
+        !ok_opt(err, 4))
+        return MOE_ERR_INVALID_ARG;
+    CombineArgs a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.K = s.K;
+    a.H = s.H;
+    a.epr = s.E / s.P;
+    a.S = S;
+    a.y = static_cast<const uint8_t*>(y);
+    a.y_stride = y_row_stride;
+    a.part_row_base = part_row_base;
+    a.arena_rows = arena_rows;
+    a.send_head = send_head;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.out = out;
+    a.err = err;
+    return from_cuda(launch_combine(s, a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

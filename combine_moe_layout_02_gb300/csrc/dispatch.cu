@@ -1,0 +1,335 @@
+// dispatch.cu -- the permutation into the ranks' receive partitions (moe_dispatch).
+//
+// For token g and every rank d with send_head[g][d] >= 0 the slot at row
+// part_row_base[d] + send_head[g][d] receives the row (bf16 bits, or int8 +
+// fp32 scale) and the triple (source rank, source-local token, lowest k on d):
+// "HCCL Window 模式 (Non-SHMEM) 代码深度剖析", section 2.3 (slot format) and
+// section 3.6 (InputToShare: read the row once, optional dynamic quantisation
+// BF16 -> FP32 -> Abs -> ReduceMax -> Scale -> INT8, FillTriple, write out).
+// One copy per distinct destination rank: "Ascend DeepEP MoE Dispatch
+// Optimization", section "一条 token 如何走完 MoE".
+//
+// Design (sm_103a). The data path is a pure byte permutation, so it runs on the
+// bulk-copy (TMA) engine rather than on the SM's load/store pipes:
+//  * Persistent grid, one CTA per token stream (CTA b takes tokens b, b+G, ...).
+//  * A ring of `stages` shared-memory row buffers is filled by
+//    cp.async.bulk global->shared loads completing on an mbarrier; each source
+//    row is read from HBM exactly once.
+//  * bf16: for each destination, one lane issues a cp.async.bulk
+//    shared->global store of the whole row straight from the ring. Lanes own
+//    destinations d = lane, lane+32, ... A ring slot is reused once
+//    cp.async.bulk.wait_group.read shows its stores have left shared memory.
+//    Warp 0 runs the copies; the other warps write the triples and side arrays
+//    for the same tokens in parallel.
+//  * int8: all warps read the row from the ring, reduce |x| to amax (warp
+//    shuffles + one shared slot per warp), quantise with IEEE division and
+//    round-half-even into a double-buffered shared int8 row, and the same bulk
+//    stores fan that row out to the destinations.
+// Every mbarrier wait is bounded; on time-out the CTA records
+// MOE_ERR_DEVICE_TIMEOUT, drains its own copies (bounded) and returns.
+#include <cuda_bf16.h>
+
+#include "moe_device.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBf16Threads = 128;
+constexpr int kInt8Threads = 256;
+constexpr int kMaxStages = 8;
+
+struct DispatchSmem {
+    size_t prb, bars, ring, qbuf, total;
+};
+
+__host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes, int H,
+                                                      bool quant) {
+    DispatchSmem l;
+    l.prb = 0;
+    l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
+    l.ring = l.bars + 128;
+    l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
+    l.total = l.qbuf + (quant ? 2 * static_cast<size_t>(round_up(H, 128)) : 0);
+    return l;
+}
+
+// Triple + side arrays for every destination of token g; one warp.
+__device__ void write_token_meta(const DispatchArgs& a, const int64_t* prb, int64_t g, int lane) {
+    const int K = a.K;
+    int32_t idx = -1;
+    float w = 0.f;
+    if (lane < K) {
+        idx = __ldg(a.topk_idx + g * K + lane);
+        if (a.topk_weights) w = __ldg(a.topk_weights + g * K + lane);
+    }
+    const int32_t dk = (idx >= 0 && idx < a.E) ? idx / a.epr : -1;
+    const int32_t src_rank = static_cast<int32_t>(g / a.T);
+    const int32_t src_tok = static_cast<int32_t>(g % a.T);
+    for (int d0 = 0; d0 < a.P; d0 += 32) {
+        const int d = d0 + lane;
+        const int32_t sh = d < a.P ? __ldg(a.send_head + g * a.P + d) : -1;
+        uint32_t todo = __ballot_sync(0xffffffffu, sh >= 0);
+        while (todo) {
+            const int j = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int dd = d0 + j;
+            const int32_t shd = __shfl_sync(0xffffffffu, sh, j);
+            const int64_t lo = prb[dd], hi = prb[dd + 1];
+            const int64_t row = lo + shd;
+            if (shd >= hi - lo || row < 0 || row >= a.arena_rows) continue;  // reported by the copy path
+            const bool on = dk == dd;
+            const uint32_t kb = __ballot_sync(0xffffffffu, on);
+            if (lane < K) {
+                if (a.recv_topk_idx) a.recv_topk_idx[row * K + lane] = on ? idx % a.epr : -1;
+                if (a.recv_topk_weights) a.recv_topk_weights[row * K + lane] = on ? w : 0.f;
+            }
+            if (lane == 0) {
+                if (a.recv_src_idx) a.recv_src_idx[row] = src_tok;
+                const int4 triple = make_int4(src_rank, src_tok, kb ? __ffs(kb) - 1 : -1, 0);
+                *reinterpret_cast<int4*>(a.arena + row * a.stride + a.triple_off) = triple;
+            }
+        }
+    }
+}
+
+// Row address of destination d for token g, or nullptr (and an error) when the
+// row is outside its partition or the arena.
+__device__ __forceinline__ uint8_t* slot_of(const DispatchArgs& a, const int64_t* prb, int d, int32_t sh) {
+    const int64_t lo = prb[d], hi = prb[d + 1];
+    const int64_t row = lo + sh;
+    if (sh < hi - lo && row >= 0 && row < a.arena_rows) return a.arena + row * a.stride;
+    raise_error(a.err, MOE_ERR_CAPACITY);
+    return nullptr;
+}
+
+__device__ void load_prb_and_init(const DispatchArgs& a, int64_t* prb, uint64_t* bars) {
+    for (int i = threadIdx.x; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < a.stages; ++st) mbar_init(&bars[st], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+}
+
+// After a failed wait: wait (bounded) for the loads this CTA still has in flight
+// into its ring, so that no copy lands in shared memory after the CTA exits.
+__device__ void drain_loads(uint64_t* bars, int stages, int64_t first, int64_t last_issued) {
+    for (int64_t j = first; j <= last_issued; ++j) mbar_wait(&bars[j % stages], (j / stages) & 1);
+}
+
+__global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, false);
+    int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    unsigned char* ring = smem + L.ring;
+    load_prb_and_init(a, prb, bars);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t G = gridDim.x;
+    const int64_t n_local = blockIdx.x < a.S ? (a.S - 1 - blockIdx.x) / G + 1 : 0;
+
+    if (warp != 0) {
+        for (int64_t i = warp - 1; i < n_local; i += nwarps - 1)
+            write_token_meta(a, prb, blockIdx.x + i * G, lane);
+        return;
+    }
+
+    const int NS = a.stages;
+    const uint32_t RB = a.row_bytes;
+    int64_t last_issued = -1;
+    if (lane == 0) {
+        const int64_t npro = n_local < NS ? n_local : NS;
+        for (int64_t i = 0; i < npro; ++i) {
+            mbar_arrive_expect_tx(&bars[i], RB);
+            bulk_load(ring + i * RB, a.x + (blockIdx.x + i * G) * a.H, RB, &bars[i]);
+        }
+        last_issued = npro - 1;
+    }
+    __syncwarp();
+    bool failed = false;
+    int64_t i = 0;
+    for (; i < n_local; ++i) {
+        const int slot = static_cast<int>(i % NS);
+        const int64_t g = blockIdx.x + i * G;
+        const int32_t sh0 = lane < a.P ? __ldg(a.send_head + g * a.P + lane) : -1;
+        const bool ok = mbar_wait(&bars[slot], static_cast<uint32_t>((i / NS) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            failed = true;
+            break;
+        }
+        const unsigned char* src = ring + static_cast<size_t>(slot) * RB;
+        for (int d0 = 0; d0 < a.P; d0 += 32) {
+            const int d = d0 + lane;
+            const int32_t sh = d0 == 0 ? sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
+            if (sh >= 0) {
+                uint8_t* dst = slot_of(a, prb, d, sh);
+                if (dst) bulk_store(dst, src, RB);
+            }
+        }
+        bulk_commit();
+        // Token i-1's stores have left its slot once at most one group (token
+        // i's) still reads shared memory; refill that slot.
+        bulk_wait_read<1>();
+        __syncwarp();
+        if (lane == 0 && i >= 1) {
+            const int64_t nxt = i - 1 + NS;
+            if (nxt < n_local) {
+                const int ps = static_cast<int>((i - 1) % NS);
+                mbar_arrive_expect_tx(&bars[ps], RB);
+                bulk_load(ring + static_cast<size_t>(ps) * RB, a.x + (blockIdx.x + nxt * G) * a.H, RB,
+                          &bars[ps]);
+                last_issued = nxt;
+            }
+        }
+        __syncwarp();
+    }
+    bulk_wait<0>();
+    if (failed && lane == 0) {
+        raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+        drain_loads(bars, NS, i, last_issued);
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t quant_pair(uint32_t v, float scale, bool zero) {
+    int32_t q0 = 0, q1 = 0;
+    if (!zero) {
+        q0 = __float2int_rn(__fdiv_rn(bf16_lo(v), scale));
+        q1 = __float2int_rn(__fdiv_rn(bf16_hi(v), scale));
+        q0 = max(-127, min(127, q0));
+        q1 = max(-127, min(127, q1));
+    }
+    return (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8);
+}
+
+__global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[kInt8Threads / 32];
+    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, true);
+    int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    unsigned char* ring = smem + L.ring;
+    unsigned char* qbuf = smem + L.qbuf;
+    const size_t qstride = static_cast<size_t>(round_up(a.H, 128));
+    load_prb_and_init(a, prb, bars);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int64_t G = gridDim.x;
+    const int64_t n_local = blockIdx.x < a.S ? (a.S - 1 - blockIdx.x) / G + 1 : 0;
+    const int NS = a.stages;
+    const uint32_t RB = a.row_bytes;
+    const int nchunks = a.H / 8;  // 16-byte chunks of the bf16 row
+
+    int64_t last_issued = -1;
+    if (tid == 0) {
+        const int64_t npro = n_local < NS ? n_local : NS;
+        for (int64_t i = 0; i < npro; ++i) {
+            mbar_arrive_expect_tx(&bars[i], RB);
+            bulk_load(ring + i * RB, a.x + (blockIdx.x + i * G) * a.H, RB, &bars[i]);
+        }
+        last_issued = npro - 1;
+    }
+    bool failed = false;
+    int64_t i = 0;
+    for (; i < n_local; ++i) {
+        const int slot = static_cast<int>(i % NS);
+        const int64_t g = blockIdx.x + i * G;
+        const bool ok = mbar_wait(&bars[slot], static_cast<uint32_t>((i / NS) & 1));
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        const uint4* row = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * RB);
+        float m = 0.f;
+        for (int j = tid; j < nchunks; j += nthreads) {
+            const uint4 v = row[j];
+            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))));
+            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
+            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+        }
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        float amax = 0.f;
+        for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, red[w]);
+        const float scale = __fdiv_rn(amax, 127.0f);
+        const bool zero = amax == 0.f;
+        unsigned char* q = qbuf + static_cast<size_t>(i & 1) * qstride;
+        for (int j = tid; j < nchunks; j += nthreads) {
+            const uint4 v = row[j];
+            uint2 packed;
+            packed.x = quant_pair(v.x, scale, zero) | (quant_pair(v.y, scale, zero) << 16);
+            packed.y = quant_pair(v.z, scale, zero) | (quant_pair(v.w, scale, zero) << 16);
+            reinterpret_cast<uint2*>(q)[j] = packed;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // The ring slot has been read by every thread: refill it.
+        if (tid == 0) {
+            const int64_t nxt = i + NS;
+            if (nxt < n_local) {
+                mbar_arrive_expect_tx(&bars[slot], RB);
+                bulk_load(ring + static_cast<size_t>(slot) * RB, a.x + (blockIdx.x + nxt * G) * a.H, RB,
+                          &bars[slot]);
+                last_issued = nxt;
+            }
+        }
+        for (int d = tid; d < a.P; d += nthreads) {
+            const int32_t sh = __ldg(a.send_head + g * a.P + d);
+            if (sh >= 0) {
+                uint8_t* dst = slot_of(a, prb, d, sh);
+                if (dst) {
+                    bulk_store(dst, q, static_cast<uint32_t>(a.H));
+                    *reinterpret_cast<float*>(dst + a.scale_off) = scale;
+                }
+            }
+        }
+        bulk_commit();
+        if (warp == static_cast<int>(i % nwarps)) write_token_meta(a, prb, g, lane);
+        // The int8 buffer written two tokens from now is this token's partner:
+        // its stores must have left shared memory before then.
+        bulk_wait_read<1>();
+    }
+    bulk_wait<0>();
+    if (failed && tid == 0) {
+        raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+        drain_loads(bars, NS, i, last_issued);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
+    if (a.S == 0) return cudaSuccess;
+    const bool quant = s.quant != 0;
+    // Ring depth: as many rows as fit in ~96 KB, between 2 and kMaxStages.
+    int stages = static_cast<int>((96 * 1024) / a.row_bytes);
+    stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
+    a.stages = stages;
+    const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
+    const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel)
+                           : reinterpret_cast<const void*>(dispatch_bf16_kernel);
+    const int threads = quant ? kInt8Threads : kBf16Threads;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L.total));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, L.total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+    if (grid > a.S) grid = a.S;
+    if (quant)
+        dispatch_int8_kernel<<<static_cast<unsigned>(grid), threads, L.total, stream>>>(a);
+    else
+        dispatch_bf16_kernel<<<static_cast<unsigned>(grid), threads, L.total, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,246 @@
+"""ctypes binding of libmoe.so (include/moe.h): argument marshalling only.
+
+Every function here forwards torch tensors' device pointers and the current
+CUDA stream to the C ABI of the same name; all work runs in the library's
+sm_103a kernels. A non-zero status raises :class:`MoeError`. If the library
+has not been built, the first call raises -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_TOPK_OUT_OF_RANGE = 2
+MOE_ERR_CAPACITY = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_UNSUPPORTED = 5
+MOE_ERR_DEVICE_TIMEOUT = 6
+MOE_ERR_INCONSISTENT = 7
+
+EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
+           "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int32), ("E", ctypes.c_int32), ("S", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("H", ctypes.c_int32), ("num_channels", ctypes.c_int32),
+                ("expert_alignment", ctypes.c_int32), ("quant", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "moe_shape(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+def make_shape(P, E, S, K, H, num_channels=16, expert_alignment=1, quant=0) -> moe_shape:
+    return moe_shape(P, E, S, K, H, num_channels, expert_alignment, quant)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Open libmoe.so (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+    try:  # torch's CUDA runtime satisfies libmoe's libcudart dependency
+        import torch  # noqa: F401
+    except ImportError:  # pragma: no cover
+        pass
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sp = ctypes.POINTER(moe_shape)
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_status_string.argtypes = [i32]
+    L.moe_check_shape.restype = i32
+    L.moe_check_shape.argtypes = [sp]
+    L.moe_slot_stride.restype = i64
+    L.moe_slot_stride.argtypes = [i32, i32]
+    L.moe_scratch_bytes.restype = i64
+    L.moe_scratch_bytes.argtypes = [sp]
+    L.moe_max_recv_rows.restype = i64
+    L.moe_max_recv_rows.argtypes = [sp]
+    L.moe_layout.restype = i32
+    L.moe_layout.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, i64, vp]
+    L.moe_notify.restype = i32
+    L.moe_notify.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp]
+    L.moe_dispatch.restype = i32
+    L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
+    L.moe_combine.restype = i32
+    L.moe_combine.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    """Device pointer of a tensor (None -> NULL). Accepts raw ints too."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status, where):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def moe_check_shape(shape: moe_shape) -> int:
+    return int(lib().moe_check_shape(ctypes.byref(shape)))
+
+
+def moe_slot_stride(H: int, quant: int) -> int:
+    return int(lib().moe_slot_stride(int(H), int(quant)))
+
+
+def moe_scratch_bytes(shape: moe_shape) -> int:
+    return int(lib().moe_scratch_bytes(ctypes.byref(shape)))
+
+
+def moe_max_recv_rows(shape: moe_shape) -> int:
+    return int(lib().moe_max_recv_rows(ctypes.byref(shape)))
+
+
+def moe_layout(shape, topk_idx, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+               is_token_in_rank_bits, err, scratch, stream=None):
+    st = lib().moe_layout(ctypes.byref(shape), _ptr(topk_idx), _ptr(num_tokens_per_rank),
+                          _ptr(num_tokens_per_expert), _ptr(is_token_in_rank),
+                          _ptr(is_token_in_rank_bits), _ptr(err), _ptr(scratch),
+                          int(scratch.numel() * scratch.element_size()), _stream(stream))
+    _check(st, "moe_layout")
+
+
+def moe_notify(shape, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+               rank_prefix_matrix, channel_prefix_matrix, recv_channel_prefix_matrix,
+               num_recv_tokens, num_recv_tokens_per_expert, recv_expert_offset, send_head,
+               part_row_base, scratch, stream=None):
+    st = lib().moe_notify(ctypes.byref(shape), _ptr(num_tokens_per_rank), _ptr(num_tokens_per_expert),
+                          _ptr(is_token_in_rank), _ptr(rank_prefix_matrix),
+                          _ptr(channel_prefix_matrix), _ptr(recv_channel_prefix_matrix),
+                          _ptr(num_recv_tokens), _ptr(num_recv_tokens_per_expert),
+                          _ptr(recv_expert_offset), _ptr(send_head), _ptr(part_row_base),
+                          _ptr(scratch), int(scratch.numel() * scratch.element_size()),
+                          _stream(stream))
+    _check(st, "moe_notify")
+
+
+def moe_dispatch(shape, x, topk_idx, topk_weights, send_head, part_row_base, recv_arena, arena_rows,
+                 recv_src_idx, recv_topk_idx, recv_topk_weights, err, stream=None):
+    st = lib().moe_dispatch(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(topk_weights),
+                            _ptr(send_head), _ptr(part_row_base), _ptr(recv_arena), int(arena_rows),
+                            _ptr(recv_src_idx), _ptr(recv_topk_idx), _ptr(recv_topk_weights),
+                            _ptr(err), _stream(stream))
+    _check(st, "moe_dispatch")
+
+
+def moe_combine(shape, y, y_row_stride, part_row_base, arena_rows, send_head, topk_idx,
+                topk_weights, out, err, stream=None):
+    st = lib().moe_combine(ctypes.byref(shape), _ptr(y), int(y_row_stride), _ptr(part_row_base),
+                           int(arena_rows), _ptr(send_head), _ptr(topk_idx), _ptr(topk_weights),
+                           _ptr(out), _ptr(err), _stream(stream))
+    _check(st, "moe_combine")
+
+
+class Buffers:
+    """Device buffers for one shape, allocated with torch (memory only).
+
+    ``arena_rows`` defaults to :func:`moe_max_recv_rows`, which always holds
+    the packed partitions moe_notify lays out, so no host read-back of the
+    receive counts is needed before dispatch.
+    """
+
+    def __init__(self, shape: moe_shape, device="cuda", arena_rows: int | None = None,
+                 side_arrays: bool = True, bits: bool = True):
+        import torch
+
+        P, E, S, K, H, C = shape.P, shape.E, shape.S, shape.K, shape.H, shape.num_channels
+        self.shape = shape
+        self.device = device
+        i32, dev = torch.int32, device
+        self.num_tokens_per_rank = torch.empty((P, P), dtype=i32, device=dev)
+        self.num_tokens_per_expert = torch.empty((P, E), dtype=i32, device=dev)
+        self.is_token_in_rank = torch.empty((S, P), dtype=torch.uint8, device=dev)
+        self.is_token_in_rank_bits = (torch.empty((S, (P + 31) // 32), dtype=i32, device=dev)
+                                      if bits else None)
+        self.err = torch.zeros((4,), dtype=i32, device=dev)
+        self.scratch = torch.empty((max(moe_scratch_bytes(shape), 256),), dtype=torch.uint8, device=dev)
+        self.rank_prefix_matrix = torch.empty((P, P), dtype=i32, device=dev)
+        self.channel_prefix_matrix = torch.empty((P, P, C), dtype=i32, device=dev)
+        self.recv_channel_prefix_matrix = torch.empty((P, P, C), dtype=i32, device=dev)
+        self.num_recv_tokens = torch.empty((P,), dtype=i32, device=dev)
+        self.num_recv_tokens_per_expert = torch.empty((P, E // P), dtype=i32, device=dev)
+        self.recv_expert_offset = torch.empty((P, E // P), dtype=i32, device=dev)
+        self.send_head = torch.empty((S, P), dtype=i32, device=dev)
+        self.part_row_base = torch.empty((P + 1,), dtype=torch.int64, device=dev)
+        self.arena_rows = moe_max_recv_rows(shape) if arena_rows is None else int(arena_rows)
+        self.stride = moe_slot_stride(H, shape.quant)
+        self.recv_arena = torch.empty((max(self.arena_rows, 1), self.stride), dtype=torch.uint8, device=dev)
+        if side_arrays:
+            self.recv_src_idx = torch.empty((max(self.arena_rows, 1),), dtype=i32, device=dev)
+            self.recv_topk_idx = torch.empty((max(self.arena_rows, 1), K), dtype=i32, device=dev)
+            self.recv_topk_weights = torch.empty((max(self.arena_rows, 1), K), dtype=torch.float32,
+                                                 device=dev)
+        else:
+            self.recv_src_idx = self.recv_topk_idx = self.recv_topk_weights = None
+
+    def layout(self, topk_idx, stream=None):
+        moe_layout(self.shape, topk_idx, self.num_tokens_per_rank, self.num_tokens_per_expert,
+                   self.is_token_in_rank, self.is_token_in_rank_bits, self.err, self.scratch, stream)
+
+    def notify(self, stream=None):
+        moe_notify(self.shape, self.num_tokens_per_rank, self.num_tokens_per_expert,
+                   self.is_token_in_rank, self.rank_prefix_matrix, self.channel_prefix_matrix,
+                   self.recv_channel_prefix_matrix, self.num_recv_tokens,
+                   self.num_recv_tokens_per_expert, self.recv_expert_offset, self.send_head,
+                   self.part_row_base, self.scratch, stream)
+
+    def dispatch(self, x, topk_idx, topk_weights, stream=None):
+        moe_dispatch(self.shape, x, topk_idx, topk_weights, self.send_head, self.part_row_base,
+                     self.recv_arena, self.arena_rows, self.recv_src_idx, self.recv_topk_idx,
+                     self.recv_topk_weights, self.err, stream)
+
+    def combine(self, out, topk_idx, topk_weights, y=None, y_row_stride=None, stream=None):
+        """Combine; by default y is the dispatch arena (identity experts)."""
+        if y is None:
+            y, y_row_stride = self.recv_arena, self.stride
+        moe_combine(self.shape, y, y_row_stride, self.part_row_base, self.arena_rows, self.send_head,
+                    topk_idx, topk_weights, out, self.err, stream)
+
+    def step(self, x, topk_idx, topk_weights, out, stream=None):
+        """One pass of the hot path: layout -> notify -> dispatch -> combine."""
+        self.layout(topk_idx, stream)
+        self.notify(stream)
+        self.dispatch(x, topk_idx, topk_weights, stream)
+        self.combine(out, topk_idx, topk_weights, stream=stream)

@@ -1,0 +1,229 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the GB300 (sm_103a) MoE dispatch/combine path.
+ *
+ * The path moves the hidden rows of S tokens to the expert-parallel ranks that
+ * own their Top-K experts and reduces the experts' answers back:
+ *
+ *   moe_layout   topk_idx            -> per-rank / per-expert counts, token->rank table
+ *   moe_notify   counts + table      -> prefix matrices, receive offsets, send_head
+ *   moe_dispatch x + send_head       -> receive slots in P rank partitions (+ side arrays)
+ *   moe_combine  expert rows (y)     -> out[S,H] = weighted sum over ranks
+ *
+ * The P expert-parallel ranks are P disjoint partitions of one receive arena
+ * in this GPU's memory; "sending" a row to rank d means storing it in d's
+ * partition. Source rank s owns global tokens [s*T, (s+1)*T), T = S / P.
+ *
+ * Problem statement followed ("Ascend DeepEP MoE Dispatch Optimization",
+ * section "一条 token 如何走完 MoE"): inputs x[S,H], topk_idx[S,K],
+ * topk_weights[S,K]; dst_rank = expert_id / experts_per_rank and
+ * dst_local_expert = expert_id % experts_per_rank; one copy of the row per
+ * distinct destination rank; combine returns the rows and reduces them by the
+ * Top-K weights.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers, owned and allocated by the
+ *     caller. The library never allocates device or pinned memory.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns; results are ready when the stream
+ *     reaches them. Nothing synchronises with the host.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED and enqueues
+ *     nothing. MOE_ERR_CUDA means a launch failed.
+ *   - Data-dependent problems (an expert id >= E, a receive row outside its
+ *     partition or the arena, an inconsistent send_head) cannot be seen on the
+ *     host. The kernels skip the offending element -- they never read or
+ *     write out of bounds -- and store a moe_status code into the caller's
+ *     device word `err` (may be NULL). moe_layout always writes `err` (0 or a
+ *     code); the later calls only ever write a non-zero code into it.
+ *   - Row-major layouts; int32 counts; the bf16 payload is passed as uint16
+ *     bit patterns.
+ *   - Alignment: every array pointer must be 16-byte aligned (the error word
+ *     4-byte, scratch 256-byte); allocations from cudaMalloc or the PyTorch
+ *     caching allocator are 256-byte aligned. y_row_stride is a multiple of 16.
+ *   - Results are deterministic: the same inputs give the same bits on every
+ *     run (no floating-point atomics, fixed reduction orders).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* bad pointer, size, alignment or shape      */
+    MOE_ERR_TOPK_OUT_OF_RANGE = 2,  /* device: an expert id was >= E              */
+    MOE_ERR_CAPACITY = 3,           /* device: a receive row fell outside its partition or the arena */
+    MOE_ERR_CUDA = 4,               /* a CUDA launch or attribute call failed     */
+    MOE_ERR_UNSUPPORTED = 5,        /* shape beyond the limits below              */
+    MOE_ERR_DEVICE_TIMEOUT = 6,     /* device: a bounded wait on a copy gave up   */
+    MOE_ERR_INCONSISTENT = 7        /* device: send_head names more ranks than the token's experts allow */
+} moe_status;
+
+/* Limits (the pages' CAM limits are P <= 384, E <= 512, K <= 16, H <= 7168). */
+#define MOE_MAX_RANKS 1024
+#define MOE_MAX_EXPERTS 4096
+#define MOE_MAX_TOPK 16
+#define MOE_MAX_HIDDEN 16384
+
+/* Shape of one call. The tiling record of "HCCL Window 模式 (Non-SHMEM)
+ * 代码深度剖析", section 8.1 (epWorldSize, moeExpertNum, quantMode, bs, k, h)
+ * reduced to what the path needs. */
+typedef struct moe_shape {
+    int32_t P;                 /* expert-parallel ranks, 1..MOE_MAX_RANKS                  */
+    int32_t E;                 /* experts, E % P == 0, P <= E <= MOE_MAX_EXPERTS            */
+    int32_t S;                 /* global tokens, S % P == 0 (T = S / P per source rank), >= 0 */
+    int32_t K;                 /* Top-K slots per token, 1..MOE_MAX_TOPK                    */
+    int32_t H;                 /* hidden size, multiple of 8 (of 16 when quant = 1)          */
+    int32_t num_channels;      /* C >= 1: shapes the channel prefix matrices only           */
+    int32_t expert_alignment;  /* >= 1: per-expert receive counts are rounded up to it      */
+    int32_t quant;             /* 0: bf16 payload; 1: int8 payload + fp32 scale             */
+} moe_shape;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int32_t status);
+
+/* Host-side check of a shape against the rules above. */
+moe_status moe_check_shape(const moe_shape* shape);
+
+/* Bytes per receive slot ("HCCL Window 模式 (Non-SHMEM) 代码深度剖析",
+ * section 2.3 token format and section 8.2 size check):
+ *   Ceil(Ceil(H * elt, 32) + 44, 512), elt = 2 (bf16) or 1 (int8).
+ * Slot layout: payload [0, H*elt); fp32 scale at byte Ceil(H*elt, 32)
+ * (int8 only); int32 triple (source rank, source-local token, lowest k whose
+ * expert is on this rank) at byte Ceil(H*elt, 32) + 32 (16 bytes written, the
+ * last 4 are zero); the rest is padding and is not written.
+ * 14848 bytes for H = 7168 bf16. Returns -1 for H < 1. */
+int64_t moe_slot_stride(int32_t H, int32_t quant);
+
+/* Scratch bytes moe_layout and moe_notify need for this shape (the two calls
+ * may share one buffer; its contents do not carry over between calls). */
+int64_t moe_scratch_bytes(const moe_shape* shape);
+
+/* Receive rows that always suffice when partitions are packed back to back
+ * (part_row_base from moe_notify): S * min(K, P). */
+int64_t moe_max_recv_rows(const moe_shape* shape);
+
+/*
+ * moe_layout -- the routing tables ("Ascend DeepEP MoE Dispatch
+ * Optimization", sections "从 Python 接口进入真实调用链" and "Dispatch handle
+ * 六项分别保存什么": num_tokens_per_rank, num_tokens_per_expert and the [S,P]
+ * boolean is_token_in_rank).
+ *
+ *   topk_idx               int32 [S,K]  expert ids; any negative value is a
+ *                                       masked slot; ids >= E are skipped and
+ *                                       reported as MOE_ERR_TOPK_OUT_OF_RANGE
+ *   num_tokens_per_rank    int32 [P,P]  [s][d] = tokens of source rank s with
+ *                                       at least one expert on rank d
+ *   num_tokens_per_expert  int32 [P,E]  [s][e] = slots of s's tokens equal to e
+ *   is_token_in_rank       uint8 [S,P]  1 if token g has an expert on rank d
+ *   is_token_in_rank_bits  uint32 [S,ceil(P/32)] or NULL: the same table packed,
+ *                                       bit d%32 of word d/32
+ *   err                    int32 device word or NULL; always written (0 or 2)
+ *   scratch                >= moe_scratch_bytes(shape) bytes, 256-byte aligned
+ */
+moe_status moe_layout(const moe_shape* shape, const int32_t* topk_idx,
+                      int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                      uint8_t* is_token_in_rank, uint32_t* is_token_in_rank_bits,
+                      int32_t* err, void* scratch, int64_t scratch_bytes, void* stream);
+
+/*
+ * moe_notify -- counts and prefixes ("Ascend DeepEP MoE Dispatch
+ * Optimization", section "Notify 先交换数量和前缀"; per-expert alignment from
+ * "internode.cu", section 1 notify_dispatch; receive position from section
+ * "Device 侧如何把 channel 变成远端 Put").
+ *
+ *   inputs: num_tokens_per_rank [P,P], num_tokens_per_expert [P,E],
+ *           is_token_in_rank [S,P] (as written by moe_layout)
+ *   rank_prefix_matrix         int32 [P,P]   [s][d] = sum over s' <= s of num_tokens_per_rank[s'][d]
+ *   channel_prefix_matrix      int32 [P,P,C] [s][d][c] = tokens of s in channels 0..c bound for d
+ *                                            (channel c = c-th block of the balanced split of T
+ *                                            tokens over C, first T % C blocks one larger:
+ *                                            "HCCL Window 模式 (Non-SHMEM) 代码深度剖析", section 8.3)
+ *   recv_channel_prefix_matrix int32 [P,P,C] [d][s][c] = first row of (s, c)'s tokens in d's partition
+ *   num_recv_tokens            int32 [P]     rows received by each rank
+ *   num_recv_tokens_per_expert int32 [P,E/P] slots per local expert, rounded up to expert_alignment
+ *   recv_expert_offset         int32 [P,E/P] exclusive scan of the line above, per rank
+ *   send_head                  int32 [S,P]   row of token g inside d's partition, or -1 if not sent:
+ *                                            rank_prefix[s-1][d] + channel_prefix[s][d][c-1] +
+ *                                            running count inside the channel
+ *   part_row_base              int64 [P+1]   exclusive scan of num_recv_tokens: partitions packed
+ *                                            back to back; part_row_base[P] = total rows
+ *   scratch                    >= moe_scratch_bytes(shape) bytes, 256-byte aligned
+ */
+moe_status moe_notify(const moe_shape* shape, const int32_t* num_tokens_per_rank,
+                      const int32_t* num_tokens_per_expert, const uint8_t* is_token_in_rank,
+                      int32_t* rank_prefix_matrix, int32_t* channel_prefix_matrix,
+                      int32_t* recv_channel_prefix_matrix, int32_t* num_recv_tokens,
+                      int32_t* num_recv_tokens_per_expert, int32_t* recv_expert_offset,
+                      int32_t* send_head, int64_t* part_row_base,
+                      void* scratch, int64_t scratch_bytes, void* stream);
+
+/*
+ * moe_dispatch -- the permutation ("HCCL Window 模式 (Non-SHMEM) 代码深度剖析",
+ * section 3.6 InputToShare with the dynamic quantisation steps and FillTriple;
+ * one copy per distinct rank as in "Ascend DeepEP MoE Dispatch Optimization").
+ *
+ * For every token g and rank d with send_head[g][d] >= 0, slot row
+ * part_row_base[d] + send_head[g][d] of the arena receives:
+ *   quant = 0: the bf16 row x[g], bit for bit;
+ *   quant = 1: q[h] = clamp(rint(f32(x[g][h]) / scale), -127, 127) as int8 and
+ *              scale = amax / 127 (binary32, round to nearest even; amax = max|x[g]|;
+ *              amax == 0 gives scale 0 and q 0);
+ *   the triple (g / T, g % T, lowest k with topk_idx[g][k] / (E/P) == d).
+ * Side arrays (each may be NULL), indexed by arena row:
+ *   recv_src_idx      int32 [arena_rows]    g % T
+ *   recv_topk_idx     int32 [arena_rows,K]  topk_idx % (E/P) where the expert is on d, else -1
+ *   recv_topk_weights float [arena_rows,K]  topk_weights where the expert is on d, else 0
+ *
+ *   x                bf16 bits [S,H], 16-byte aligned
+ *   topk_idx         int32 [S,K]; topk_weights float [S,K] (may be NULL when
+ *                    recv_topk_weights is NULL)
+ *   part_row_base    int64 [P+1] device: first arena row of each partition;
+ *                    moe_notify's packed bases, or any caller-chosen bases
+ *                    (e.g. d * capacity for fixed-capacity partitions)
+ *   recv_arena       arena_rows * moe_slot_stride(H, quant) bytes, 16-byte aligned
+ *   err              int32 device word or NULL: rows outside [part_row_base[d],
+ *                    part_row_base[d+1]) or beyond arena_rows are skipped and
+ *                    raise MOE_ERR_CAPACITY
+ */
+moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                        const float* topk_weights, const int32_t* send_head,
+                        const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,
+                        int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                        int32_t* err, void* stream);
+
+/*
+ * moe_combine -- the inverse permutation and weighted reduction ("HCCL Window
+ * 模式 (Non-SHMEM) 代码深度剖析", section 7.8 ReadBufferAndWeightedSum: FP32
+ * accumulator, Cast -> Muls -> Add per returned row, one CAST_RINT to BF16).
+ *
+ *   out[g][h] = bf16_rne( sum over d ascending with send_head[g][d] >= 0 of
+ *                         c[g][d] * f32(y[part_row_base[d] + send_head[g][d]][h]) )
+ *   c[g][d]   = sum, in ascending k, of topk_weights[g][k] over the slots whose
+ *               expert is on d; 1 for every rank when topk_weights is NULL.
+ * The accumulator starts at +0.0f; each product and each sum is rounded to
+ * binary32 on its own (no fused multiply-add). A token with no valid rank
+ * gives +0.
+ *
+ *   y             bf16 rows, y_row_stride bytes apart (a multiple of 16, >= 2H);
+ *                 pass the dispatch arena with moe_slot_stride(H, 0) for
+ *                 identity experts
+ *   part_row_base int64 [P+1] device, as for moe_dispatch; arena_rows bounds the rows read
+ *   send_head     int32 [S,P]; topk_idx int32 [S,K]; topk_weights float [S,K] or NULL
+ *   out           bf16 bits [S,H], 16-byte aligned
+ *   err           int32 device word or NULL (MOE_ERR_CAPACITY, MOE_ERR_INCONSISTENT)
+ */
+moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stride,
+                       const int64_t* part_row_base, int64_t arena_rows,
+                       const int32_t* send_head, const int32_t* topk_idx,
+                       const float* topk_weights, uint16_t* out, int32_t* err, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MOE_H_ */

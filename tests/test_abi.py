@@ -1,0 +1,67 @@
+"""The C-ABI library loads here (no GPU) and exports every declared symbol;
+host-side helpers and argument checks answer without touching a device."""
+
+import os
+import re
+
+import pytest
+
+from combine_moe_layout_02_gb300 import build as moe_build
+from combine_moe_layout_02_gb300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.lib()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moe_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"moe_layout", "moe_notify", "moe_dispatch", "moe_combine"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(moe.EXPORTS) >= names
+
+
+def test_slot_stride_and_limits(lib):
+    assert moe.moe_slot_stride(7168, 0) == 14848
+    assert moe.moe_slot_stride(7168, 1) == 7680
+    assert moe.moe_slot_stride(256, 0) == 1024
+    assert moe.moe_slot_stride(0, 0) == -1
+    ok = moe.make_shape(8, 256, 32768, 8, 7168)
+    assert moe.moe_check_shape(ok) == moe.MOE_OK
+    assert moe.moe_max_recv_rows(ok) == 32768 * 8
+    assert moe.moe_scratch_bytes(ok) >= 8 * 16 * 8 * 4
+    assert moe.moe_check_shape(moe.make_shape(8, 250, 32768, 8, 7168)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32767, 8, 7168)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 17, 7168)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 8, 7164)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 8, 7176, quant=1)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_shape(moe.make_shape(2048, 4096, 2048, 8, 64)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 0, 8, 7168)) == moe.MOE_OK
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    s = moe.make_shape(4, 16, 256, 2, 256)
+    assert lib.moe_layout(s, None, None, None, None, None, None, None, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_notify(s, *([None] * 12), 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(s, None, None, None, None, None, None, 0, None, None, None, None,
+                            None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(s, None, 512, None, 0, None, None, None, None, None,
+                           None) == moe.MOE_ERR_INVALID_ARG
+    # Misaligned (non-NULL) pointers are rejected on the host as well.
+    assert lib.moe_combine(s, 8, 512, 16, 1, 16, 16, None, 16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"

@@ -1,0 +1,200 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact for layout, notify, dispatch payload / scale / triple and side
+arrays; combine within 1 bf16 ulp of the oracle (and, since both sides round
+each product and sum in binary32 in the same order, bit-exact as well).
+"""
+
+import numpy as np
+import pytest
+
+from combine_moe_layout_02_gb300 import inputs, moe
+from tests import gpu_path as gp
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_all(w, quant=0, weights=True, y_mode="identity", sample=None, seed=0):
+    gpu = gp.run_gpu(w, quant=quant, weights=weights, y_mode=y_mode)
+    lay, nt = gp.oracle_tables(w)
+    assert gpu["layout_err"] == 0 and gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
+    gp.assert_tables_equal(gpu, lay, nt)
+    tokens = None
+    if sample is not None and sample < w.S:
+        rng = np.random.default_rng(seed)
+        tokens = np.sort(rng.choice(w.S, size=sample, replace=False))
+        tokens[0], tokens[-1] = 0, w.S - 1   # first and last token always in
+        tokens = np.unique(tokens)
+    gp.compare_dispatch(w, quant, gpu, nt, tokens=tokens)
+    gp.compare_combine(w, gpu, nt, tokens=tokens, weights=weights)
+    return gpu, lay, nt
+
+
+# ---- small sizes: whole outputs compared, several tiles and a ragged tail ----
+
+@pytest.mark.parametrize("quant", [0, 1])
+def test_tiny(quant):
+    w = inputs.workload("tiny_p4_e16_h256")
+    _check_all(w, quant=quant, y_mode="int8expert" if quant else "identity")
+
+
+@pytest.mark.parametrize("name,T", [
+    ("p8_e256_t4096_h7168", 300),            # ragged against 256-token tiles and 16 channels
+    ("p128_e256_t512_h7168_zipf", 9),        # skewed, masked, tiny channels
+    ("p32_e256_t128_h1024", 128),
+    ("p32_e256_t128_h2048", 37),
+])
+def test_reduced_workloads(name, T):
+    w = inputs.workload(name, T=T)
+    _check_all(w)
+
+
+def test_reduced_int8_with_expert_stage():
+    w = inputs.workload("p8_e256_t4096_h7168_int8", T=300)
+    _check_all(w, quant=1, y_mode="int8expert")
+
+
+def test_random_expert_rows_and_unit_weights():
+    w = inputs.workload("p32_e256_t128_h1024", T=40)
+    _check_all(w, y_mode="random")
+    _check_all(w, y_mode="random", weights=False)
+
+
+@pytest.mark.parametrize("P,E,T,K,H,C,A", [
+    (1, 8, 333, 4, 64, 16, 1),        # one rank: every token goes to rank 0
+    (3, 12, 50, 4, 136, 5, 3),        # P not a multiple of 4 (byte paths), odd C, alignment 3
+    (5, 5, 77, 5, 8, 200, 1),         # one expert per rank, more channels than tokens, H = 8
+    (1024, 1024, 2, 16, 64, 2, 1),    # maximum ranks and Top-K
+    (16, 4096, 20, 8, 16384, 16, 8),  # maximum experts and hidden size
+    (64, 128, 3, 1, 32, 1, 1),        # K = 1, one channel
+])
+def test_edge_shapes(P, E, T, K, H, C, A):
+    w = inputs.make(P, E, T, H, K, seed=P + K, mask_frac=0.05, C=C, expert_alignment=A)
+    _check_all(w)
+
+
+def test_edge_shapes_int8():
+    w = inputs.make(3, 12, 50, 16 * 9, 4, seed=3, C=5)
+    _check_all(w, quant=1, y_mode="int8expert")
+
+
+def test_empty_input():
+    w = inputs.make(4, 16, 0, 256, 2)
+    gpu = gp.run_gpu(w)
+    assert gpu["layout_err"] == 0
+    assert gpu["num_tokens_per_rank"].sum() == 0 and gpu["num_tokens_per_expert"].sum() == 0
+    assert gpu["part_row_base"].tolist() == [0] * 5
+    assert gpu["channel_prefix_matrix"].sum() == 0
+
+
+def test_all_masked_and_duplicates():
+    w = inputs.make(8, 64, 40, 128, 6, seed=4)
+    idx = w.topk_idx.copy()
+    idx[:13] = -1                      # tokens with no destination
+    idx[20:, 1] = idx[20:, 0]          # duplicate expert ids inside a row
+    w.topk_idx = idx
+    gpu, lay, nt = _check_all(w)
+    assert (gpu["out"][:13] == 0).all()  # +0 for tokens that went nowhere
+
+
+def test_zero_rows_quantise_to_zero():
+    w = inputs.make(4, 16, 32, 256, 2, seed=6)
+    w.x_bits[5] = 0
+    w.x_bits[9] = 0x8000   # all -0
+    _check_all(w, quant=1, y_mode="int8expert")
+
+
+def test_out_of_range_expert_ids():
+    w = inputs.make(4, 16, 64, 64, 2, seed=8)
+    bad = w.topk_idx.copy()
+    bad[3, 0] = 16
+    bad[100, 1] = 1 << 30
+    gpu = gp.run_gpu(w, topk_idx=bad)
+    assert gpu["layout_err"] == moe.MOE_ERR_TOPK_OUT_OF_RANGE
+    masked = bad.copy()
+    masked[masked >= 16] = -1
+    lay, nt = gp.oracle_tables(w, topk_idx=masked)
+    gp.assert_tables_equal(gpu, lay, nt)
+
+
+def test_fixed_capacity_partitions():
+    w = inputs.make(4, 16, 64, 128, 2, seed=10)
+    lay, nt = gp.oracle_tables(w)
+    cap = int(nt["num_recv_tokens"].max())
+    prb = np.arange(w.P + 1, dtype=np.int64) * cap
+    gpu = gp.run_gpu(w, arena_rows=cap * w.P, part_row_base=prb)
+    assert gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
+    gp.compare_dispatch(w, 0, gpu, nt, part_row_base=prb)
+    nt_cap = dict(nt, part_row_base=prb)
+    gp.compare_combine(w, gpu, nt_cap)
+
+
+def test_capacity_overflow_reported_without_stray_writes():
+    w = inputs.make(4, 16, 64, 128, 2, seed=10)
+    lay, nt = gp.oracle_tables(w)
+    cap = int(nt["num_recv_tokens"].min()) - 2
+    prb = np.arange(w.P + 1, dtype=np.int64) * cap
+    gpu = gp.run_gpu(w, arena_rows=cap * w.P, part_row_base=prb)
+    assert gpu["dispatch_err"] == moe.MOE_ERR_CAPACITY
+    gp.compare_dispatch(w, 0, gpu, nt, part_row_base=prb)
+
+
+def test_deterministic_repeat():
+    w = inputs.workload("p128_e256_t512_h7168_zipf", T=16)
+    gpu = gp.run_gpu(w, repeat=2)
+    a, b = gpu["runs"]
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_invalid_arguments_rejected_on_host():
+    import torch
+
+    w = inputs.make(4, 16, 16, 64, 2)
+    shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H)
+    buf = moe.Buffers(shape, "cuda")
+    x = torch.from_numpy(w.x_bits.view(np.int16)).cuda()
+    idx = torch.from_numpy(w.topk_idx).cuda()
+    wts = torch.from_numpy(w.topk_weights).cuda()
+    buf.layout(idx)
+    buf.notify()
+    xbig = torch.zeros(w.S * w.H + 8, dtype=torch.int16, device="cuda")
+    misaligned = xbig.data_ptr() + 2
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_dispatch(shape, misaligned, idx, wts, buf.send_head, buf.part_row_base,
+                         buf.recv_arena, buf.arena_rows, None, None, None, buf.err)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    bad = moe.make_shape(4, 18, 16, 2, 64)   # E % P != 0
+    with pytest.raises(moe.MoeError):
+        moe.moe_layout(bad, idx, buf.num_tokens_per_rank, buf.num_tokens_per_expert,
+                       buf.is_token_in_rank, None, buf.err, buf.scratch)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe.MoeError):
+        moe.moe_layout(shape, idx, buf.num_tokens_per_rank, buf.num_tokens_per_expert,
+                       buf.is_token_in_rank, None, buf.err, small)
+    torch.cuda.synchronize()
+    buf.dispatch(x, idx, wts)   # the context is still healthy
+    torch.cuda.synchronize()
+
+
+# ---- full sizes, launch configuration of the benchmark: sampled outputs ----
+
+@pytest.mark.parametrize("name,quant,y_mode", [
+    ("p8_e256_t4096_h7168", 0, "identity"),
+    ("p8_e256_t4096_h7168_int8", 1, "int8expert"),
+    ("p128_e256_t512_h7168_zipf", 0, "identity"),
+    ("p32_e256_t128_h7168", 0, "identity"),
+    ("p32_e256_t128_h1024", 0, "identity"),
+])
+def test_full_size_sampled(name, quant, y_mode):
+    w = inputs.workload(name)
+    gpu, lay, nt = _check_all(w, quant=quant, y_mode=y_mode, sample=1500)
+    # Whole-array properties at full size.
+    assert gpu["part_row_base"][-1] == gpu["is_token_in_rank"].sum()
+    if y_mode == "identity":
+        # Softmax weights with identity experts return x (ties of -0 become +0).
+        from tests.helpers import bf16_ulp_distance
+        d = bf16_ulp_distance(gpu["out"], w.x_bits)
+        masked_any = (w.topk_idx < 0).any()
+        if not masked_any:
+            assert d.max() <= 1
