@@ -228,10 +228,12 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(name):
+def workload_config(name, T=None):
     from combine_moe_layout_02_gb300 import inputs
 
     c = dict(inputs.WORKLOADS[name])
+    if T is not None:
+        c["T"] = T
     return {"workload": name, "P": c["P"], "E": c["E"], "S": c["P"] * c["T"], "H": c["H"],
             "K": c["K"], "routing": c["routing"], "quant": c["quant"],
             "num_channels": inputs.NUM_CHANNELS,
@@ -249,7 +251,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = inputs.workload(args.workload)
+    w = inputs.workload(args.workload, T=args.tokens_per_rank)
     shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, w.quant)
     buf = moe.Buffers(shape, dev, side_arrays=True)
     x_host = torch.from_numpy(w.x_bits.view(np.int16)).pin_memory()
@@ -356,7 +358,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(args.workload),
+        "config": workload_config(args.workload, args.tokens_per_rank),
         "gpu_launches": 6 * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
@@ -389,6 +391,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--tokens-per-rank", type=int, default=None,
+                    help="override T (a smaller case of the same workload, e.g. for profiling)")
     ap.add_argument("--ref-tokens", type=int, default=512,
                     help="tokens per rank of the oracle's bounded sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
