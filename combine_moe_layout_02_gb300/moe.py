@@ -24,7 +24,11 @@ MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_ERR_INCONSISTENT = 7
 
 EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
-           "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine")
+           "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
+           "moe_layout_static_scratch")
+
+# Bytes of the scratch buffer built into the library (include/moe.h).
+MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class MoeError(RuntimeError):
@@ -81,6 +85,8 @@ def lib() -> ctypes.CDLL:
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_combine.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+    L.moe_layout_static_scratch.restype = i32
+    L.moe_layout_static_scratch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -171,6 +177,17 @@ def moe_combine(shape, y, y_row_stride, part_row_base, arena_rows, send_head, to
                            int(arena_rows), _ptr(send_head), _ptr(topk_idx), _ptr(topk_weights),
                            _ptr(out), _ptr(err), _stream(stream))
     _check(st, "moe_combine")
+
+
+def moe_layout_static_scratch(shape, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
+                              is_token_in_rank, is_token_in_rank_bits, err, stream=None):
+    """moe_layout using the library's built-in scratch buffer: for callers that
+    cannot allocate device memory (see include/moe.h). Calls must not overlap
+    on the GPU; the first call on a device must precede any stream capture."""
+    st = lib().moe_layout_static_scratch(ctypes.byref(shape), _ptr(topk_idx), _ptr(num_tokens_per_rank),
+                                         _ptr(num_tokens_per_expert), _ptr(is_token_in_rank),
+                                         _ptr(is_token_in_rank_bits), _ptr(err), _stream(stream))
+    _check(st, "moe_layout_static_scratch")
 
 
 class Buffers:

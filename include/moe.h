@@ -222,6 +222,32 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
                        const int32_t* send_head, const int32_t* topk_idx,
                        const float* topk_weights, uint16_t* out, int32_t* err, void* stream);
 
+/*
+ * moe_layout_static_scratch -- moe_layout without a caller-provided scratch
+ * buffer. The pages have no counterpart: this entry point exists for callers
+ * that cannot allocate device memory, such as code hosted by an engine that
+ * owns all device memory and forbids allocation after start-up, or serving
+ * loops where cudaMalloc would stall the device. Inputs, outputs and results
+ * are those of moe_layout; the per-block partial counts go to a buffer of
+ * MOE_LAYOUT_STATIC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Shapes whose partials need more than MOE_LAYOUT_STATIC_SCRATCH_BYTES
+ *     (moe_scratch_bytes is an upper bound) return MOE_ERR_UNSUPPORTED and
+ *     enqueue nothing.
+ *   - The first call on each device looks up the buffer's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the buffer, which keeps the last call's contents;
+ *     nothing in it needs to start at zero. Calls that overlap on the GPU
+ *     (different streams or threads) race on it: serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (1u << 20)
+moe_status moe_layout_static_scratch(const moe_shape* shape, const int32_t* topk_idx,
+                                     int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                     uint8_t* is_token_in_rank, uint32_t* is_token_in_rank_bits,
+                                     int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -65,3 +65,15 @@ def test_null_pointers_rejected_before_any_launch(lib):
     # Misaligned (non-NULL) pointers are rejected on the host as well.
     assert lib.moe_combine(s, 8, 512, 16, 1, 16, 16, None, 16, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"
+
+
+def test_static_scratch_size_guard_runs_on_the_host(lib):
+    """moe_layout_static_scratch refuses shapes beyond its built-in buffer before
+    touching any device (the fake pointers below are never dereferenced)."""
+    big = moe.make_shape(1024, 4096, 1024 * 64, 8, 64)
+    assert moe.moe_scratch_bytes(big) > moe.MOE_LAYOUT_STATIC_SCRATCH_BYTES
+    fake = 1 << 20
+    assert lib.moe_layout_static_scratch(big, fake, fake, fake, fake, fake, fake,
+                                         None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layout_static_scratch(big, None, fake, fake, fake, None, None,
+                                         None) == moe.MOE_ERR_INVALID_ARG
