@@ -12,20 +12,33 @@
 // separately (__fmul_rn / __fadd_rn), ranks are visited in ascending order,
 // so the result is the same bit pattern on every run.
 //
-// Design (sm_103a): persistent grid, one CTA per token at a time. Warp 0 turns
-// the token's send_head row into a compact list of (row address, weight) in
-// ascending rank order (ballot + popc compaction). Then every thread owns
-// 16-byte column chunks: it issues the loads of that chunk from all of the
-// token's rows before reducing them, so up to MAXR x 16 bytes per thread are in
-// flight, and writes one 16-byte chunk of out.
+// Design (sm_103a): persistent grid, one warp per token, no block barriers.
+//  * The warp compacts the token's send_head row into (row address, weight)
+//    pairs in ascending rank order (ballot, then the r-th set bit's lane hands
+//    its pair to lane r), then broadcasts the pairs to every lane once.
+//  * Each lane owns 16-byte column chunks: it issues the loads of kUnroll
+//    chunks from all of the token's rows before reducing any of them, so up to
+//    kUnroll x MAXR x 16 bytes per lane are in flight, and stores 16 bytes of
+//    out per chunk.
+//  * The routing words of the warp's next token (send_head row, Top-K ids and
+//    weights) are loaded before the current token's rows, so their latency
+//    overlaps the payload traffic.
 #include <cuda_bf16.h>
 
 #include "moe_device.cuh"
 
+#ifndef MOE_COMBINE_THREADS
+#define MOE_COMBINE_THREADS 256
+#endif
+#ifndef MOE_COMBINE_UNROLL
+#define MOE_COMBINE_UNROLL 2
+#endif
+
 namespace moe {
 namespace {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = MOE_COMBINE_THREADS;
+constexpr int kUnroll = MOE_COMBINE_UNROLL;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -37,90 +50,125 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return l | (h << 16);
 }
 
+// One lane's routing words of a token: send_head of rank `lane` (the first 32
+// ranks; further ranks are read during the compaction) and Top-K slot `lane`.
+struct TokenRoute {
+    int32_t sh0;
+    int32_t idx;
+    float w;
+};
+
+__device__ __forceinline__ TokenRoute load_route(const CombineArgs& a, int64_t g, int lane) {
+    TokenRoute r{-1, -1, 0.f};
+    if (g < a.S) {
+        if (lane < a.P) r.sh0 = __ldg(a.send_head + g * a.P + lane);
+        if (lane < a.K) {
+            r.idx = __ldg(a.topk_idx + g * a.K + lane);
+            if (a.topk_weights) r.w = __ldg(a.topk_weights + g * a.K + lane);
+        }
+    }
+    return r;
+}
+
 template <int MAXR>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_kernel(const CombineArgs a) {
     extern __shared__ __align__(16) int64_t prb[];  // [P+1]
-    __shared__ const uint8_t* s_row[MAXR];
-    __shared__ float s_coef[MAXR];
-    __shared__ int s_n;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     for (int i = tid; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
     __syncthreads();
     const int nchunks = a.H / 8;
-    const int K = a.K;
-    for (int64_t g = blockIdx.x; g < a.S; g += gridDim.x) {
-        if (warp == 0) {
-            int32_t dk = -1;
-            float w = 0.f;
-            if (lane < K) {
-                const int32_t idx = __ldg(a.topk_idx + g * K + lane);
-                dk = (idx >= 0 && idx < a.E) ? idx / a.epr : -1;
-                if (a.topk_weights) w = __ldg(a.topk_weights + g * K + lane);
+    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5);
+    TokenRoute cur = load_route(a, g, lane);
+    for (; g < a.S; g += warps_total) {
+        const TokenRoute nxt = load_route(a, g + warps_total, lane);
+        const int32_t dk = (cur.idx >= 0 && cur.idx < a.E) ? cur.idx / a.epr : -1;
+        // Compaction: lane r ends up holding the r-th valid rank's row and weight.
+        uint64_t my_row = 0;
+        float my_coef = 0.f;
+        int n = 0;
+        for (int d0 = 0; d0 < a.P; d0 += 32) {
+            const int d = d0 + lane;
+            const int32_t sh = d0 == 0 ? cur.sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
+            bool valid = false;
+            int64_t row = 0;
+            if (sh >= 0) {
+                const int64_t lo = prb[d], hi = prb[d + 1];
+                row = lo + sh;
+                valid = sh < hi - lo && row >= 0 && row < a.arena_rows;
+                if (!valid) raise_error(a.err, MOE_ERR_CAPACITY);
             }
-            int n = 0;
-            for (int d0 = 0; d0 < a.P; d0 += 32) {
-                const int d = d0 + lane;
-                const int32_t sh = d < a.P ? __ldg(a.send_head + g * a.P + d) : -1;
-                bool valid = false;
-                int64_t row = 0;
-                if (sh >= 0) {
-                    const int64_t lo = prb[d], hi = prb[d + 1];
-                    row = lo + sh;
-                    valid = sh < hi - lo && row >= 0 && row < a.arena_rows;
-                    if (!valid) raise_error(a.err, MOE_ERR_CAPACITY);
-                }
-                float c = 0.f;
-                for (int k = 0; k < K; ++k) {
-                    const int32_t dkk = __shfl_sync(0xffffffffu, dk, k);
-                    const float wk = __shfl_sync(0xffffffffu, w, k);
-                    if (dkk == d) c = __fadd_rn(c, wk);
-                }
-                if (!a.topk_weights) c = 1.f;
-                const uint32_t bal = __ballot_sync(0xffffffffu, valid);
-                if (valid) {
-                    const int pos = n + __popc(bal & lanemask_lt());
-                    if (pos < MAXR) {
-                        s_row[pos] = a.y + row * a.y_stride;
-                        s_coef[pos] = c;
-                    } else {
-                        raise_error(a.err, MOE_ERR_INCONSISTENT);
-                    }
-                }
-                n += __popc(bal);
+            float c = 0.f;
+            for (int k = 0; k < a.K; ++k) {
+                const int32_t dkk = __shfl_sync(0xffffffffu, dk, k);
+                const float wk = __shfl_sync(0xffffffffu, cur.w, k);
+                if (dkk == d) c = __fadd_rn(c, wk);
             }
-            if (lane == 0) s_n = n < MAXR ? n : MAXR;
+            if (!a.topk_weights) c = 1.f;
+            const uint64_t rp = reinterpret_cast<uint64_t>(a.y + row * a.y_stride);
+            const uint32_t bal = __ballot_sync(0xffffffffu, valid);
+            const int cnt = __popc(bal);
+            for (int r = 0; r < cnt; ++r) {
+                const int src = __fns(bal, 0, r + 1);  // lane of the (r+1)-th valid rank
+                const uint64_t p = __shfl_sync(0xffffffffu, rp, src);
+                const float cc = __shfl_sync(0xffffffffu, c, src);
+                if (lane == n + r) {
+                    my_row = p;
+                    my_coef = cc;
+                }
+            }
+            n += cnt;
         }
-        __syncthreads();
-        const int n = s_n;
+        if (n > MAXR) {
+            if (lane == 0) raise_error(a.err, MOE_ERR_INCONSISTENT);
+            n = MAXR;
+        }
+        const uint8_t* rows[MAXR];
+        float coef[MAXR];
+#pragma unroll
+        for (int r = 0; r < MAXR; ++r) {
+            rows[r] = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, my_row, r));
+            coef[r] = __shfl_sync(0xffffffffu, my_coef, r);
+        }
         uint16_t* out = a.out + g * a.H;
-        for (int j = tid; j < nchunks; j += blockDim.x) {
-            uint4 v[MAXR];
+        for (int j0 = lane; j0 < nchunks; j0 += 32 * kUnroll) {
+            uint4 v[kUnroll][MAXR];
 #pragma unroll
-            for (int r = 0; r < MAXR; ++r)
-                if (r < n) v[r] = ld_stream_u4(s_row[r] + static_cast<size_t>(j) * 16);
-            float acc[8];
+            for (int u = 0; u < kUnroll; ++u) {
+                const int j = j0 + 32 * u;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                for (int r = 0; r < MAXR; ++r)
+                    if (r < n && j < nchunks) v[u][r] = ld_stream_u4(rows[r] + static_cast<size_t>(j) * 16);
+            }
 #pragma unroll
-            for (int r = 0; r < MAXR; ++r) {
-                if (r < n) {
-                    const float c = s_coef[r];
-                    const uint32_t u[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+            for (int u = 0; u < kUnroll; ++u) {
+                const int j = j0 + 32 * u;
+                if (j < nchunks) {
+                    float acc[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(c, bf16_lo(u[q])));
-                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __fmul_rn(c, bf16_hi(u[q])));
+                    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+                    for (int r = 0; r < MAXR; ++r) {
+                        if (r < n) {
+                            const uint32_t w4[4] = {v[u][r].x, v[u][r].y, v[u][r].z, v[u][r].w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(coef[r], bf16_lo(w4[q])));
+                                acc[2 * q + 1] =
+                                    __fadd_rn(acc[2 * q + 1], __fmul_rn(coef[r], bf16_hi(w4[q])));
+                            }
+                        }
                     }
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[0], acc[1]);
+                    o.y = pack_bf16x2(acc[2], acc[3]);
+                    o.z = pack_bf16x2(acc[4], acc[5]);
+                    o.w = pack_bf16x2(acc[6], acc[7]);
+                    reinterpret_cast<uint4*>(out)[j] = o;
                 }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            reinterpret_cast<uint4*>(out)[j] = o;
         }
-        __syncthreads();
+        cur = nxt;
     }
 }
 
@@ -132,8 +180,10 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
                                                                   kCombineThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
+    const int64_t warps_per_block = kCombineThreads / 32;
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
-    if (grid > a.S) grid = a.S;
+    const int64_t needed = ceil_div(a.S, warps_per_block);
+    if (grid > needed) grid = needed;
     combine_kernel<MAXR><<<static_cast<unsigned>(grid), kCombineThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }

@@ -31,12 +31,27 @@
 
 #include "moe_device.cuh"
 
+// Tuning knobs (compile-time): shared-memory budget of the row ring, its
+// maximum depth, and how many tokens' bulk-store groups may still be reading
+// the ring when a slot is refilled.
+#ifndef MOE_DISPATCH_RING_BYTES
+#define MOE_DISPATCH_RING_BYTES (96 * 1024)
+#endif
+#ifndef MOE_DISPATCH_MAX_STAGES
+#define MOE_DISPATCH_MAX_STAGES 8
+#endif
+#ifndef MOE_DISPATCH_STORE_DEPTH
+#define MOE_DISPATCH_STORE_DEPTH 1
+#endif
+
 namespace moe {
 namespace {
 
 constexpr int kBf16Threads = 128;
 constexpr int kInt8Threads = 256;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = MOE_DISPATCH_MAX_STAGES;
+constexpr int kStoreDepth = MOE_DISPATCH_STORE_DEPTH;
+static_assert(kStoreDepth >= 1 && kStoreDepth < kMaxStages, "store depth must leave a free slot");
 
 struct DispatchSmem {
     size_t prb, bars, ring, qbuf, total;
@@ -47,7 +62,7 @@ __host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_
     DispatchSmem l;
     l.prb = 0;
     l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
-    l.ring = l.bars + 128;
+    l.ring = l.bars + static_cast<size_t>(round_up(kMaxStages * 8, 128));
     l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
     l.total = l.qbuf + (quant ? 2 * static_cast<size_t>(round_up(H, 128)) : 0);
     return l;
@@ -169,14 +184,14 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
             }
         }
         bulk_commit();
-        // Token i-1's stores have left its slot once at most one group (token
-        // i's) still reads shared memory; refill that slot.
-        bulk_wait_read<1>();
+        // Token i-D's stores have left its slot once at most D groups (tokens
+        // i-D+1 .. i) still read shared memory; refill that slot.
+        bulk_wait_read<kStoreDepth>();
         __syncwarp();
-        if (lane == 0 && i >= 1) {
-            const int64_t nxt = i - 1 + NS;
+        if (lane == 0 && i >= kStoreDepth) {
+            const int64_t nxt = i - kStoreDepth + NS;
             if (nxt < n_local) {
-                const int ps = static_cast<int>((i - 1) % NS);
+                const int ps = static_cast<int>((i - kStoreDepth) % NS);
                 mbar_arrive_expect_tx(&bars[ps], RB);
                 bulk_load(ring + static_cast<size_t>(ps) * RB, a.x + (blockIdx.x + nxt * G) * a.H, RB,
                           &bars[ps]);
@@ -308,9 +323,11 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
 cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
     if (a.S == 0) return cudaSuccess;
     const bool quant = s.quant != 0;
-    // Ring depth: as many rows as fit in ~96 KB, between 2 and kMaxStages.
-    int stages = static_cast<int>((96 * 1024) / a.row_bytes);
-    stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
+    // Ring depth: as many rows as fit in the ring budget, at least one more
+    // than the store depth (and 2), at most kMaxStages.
+    int stages = static_cast<int>(MOE_DISPATCH_RING_BYTES / a.row_bytes);
+    const int min_stages = kStoreDepth + 1 > 2 ? kStoreDepth + 1 : 2;
+    stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
     a.stages = stages;
     const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
     const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel)

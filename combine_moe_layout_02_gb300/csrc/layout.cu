@@ -138,6 +138,7 @@ layout_reduce_kernel(int32_t P, int32_t E, int64_t nbs, int64_t part_stride,
     const int32_t* base = part + s * nbs * part_stride;
     for (int j = threadIdx.x; j < P + E; j += blockDim.x) {
         int32_t sum = 0;
+#pragma unroll 8
         for (int64_t b = 0; b < nbs; ++b) sum += base[b * part_stride + j];
         if (j < P)
             ntpr[s * P + j] = sum;

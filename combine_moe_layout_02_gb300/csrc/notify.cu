@@ -62,6 +62,7 @@ __device__ void notify_prefix_block(int32_t P, int32_t E, int32_t A, const int32
     const int epr = E / P;
     for (int d = tid; d < P; d += nthreads) {
         int32_t run = 0;
+#pragma unroll 8
         for (int s = 0; s < P; ++s) {
             run += ntpr[s * P + d];
             rpm[s * P + d] = run;
@@ -71,6 +72,7 @@ __device__ void notify_prefix_block(int32_t P, int32_t E, int32_t A, const int32
     }
     for (int e = tid; e < E; e += nthreads) {
         int64_t cnt = 0;
+#pragma unroll 8
         for (int s = 0; s < P; ++s) cnt += ntpe[static_cast<int64_t>(s) * E + e];
         nrtpe[e] = static_cast<int32_t>(round_up(cnt, A));
     }
@@ -155,6 +157,7 @@ notify_head_kernel(int32_t P, int32_t C, int64_t T, const uint8_t* __restrict__ 
     split_range(T, C, c, &b, &e);
     for (int d = tid; d < P; d += nthreads) {
         int32_t pre = 0;
+#pragma unroll 8
         for (int64_t cc = 0; cc < c; ++cc) pre += ccount[(s * C + cc) * P + d];
         const int32_t cnt = ccount[(s * C + c) * P + d];
         cpm[(s * P + d) * C + c] = pre + cnt;
