@@ -209,4 +209,20 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
     return from_cuda(launch_combine(s, a, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_tokens,
+                              const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,
+                              int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                              void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (arena_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(num_recv_tokens, 1, 16) || !ok_ptr(part_row_base, 1, 16) ||
+        !ok_ptr(recv_arena, arena_rows, 16) || !ok_opt(recv_src_idx, 16) || !ok_opt(recv_topk_idx, 16) ||
+        !ok_opt(recv_topk_weights, 16))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_pad(*shape, num_recv_tokens, part_row_base, static_cast<uint8_t*>(recv_arena),
+                                arena_rows, recv_src_idx, recv_topk_idx, recv_topk_weights,
+                                static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

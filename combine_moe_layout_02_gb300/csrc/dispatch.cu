@@ -100,8 +100,11 @@ __device__ void write_token_meta(const DispatchArgs& a, const int64_t* prb, int6
             }
             if (lane == 0) {
                 if (a.recv_src_idx) a.recv_src_idx[row] = src_tok;
-                const int4 triple = make_int4(src_rank, src_tok, kb ? __ffs(kb) - 1 : -1, 0);
-                *reinterpret_cast<int4*>(a.arena + row * a.stride + a.triple_off) = triple;
+                // The triple fills its whole 32-byte sector (zero padded) so the
+                // sector never needs a read-modify-write on its way to DRAM.
+                int4* t = reinterpret_cast<int4*>(a.arena + row * a.stride + a.triple_off);
+                t[0] = make_int4(src_rank, src_tok, kb ? __ffs(kb) - 1 : -1, 0);
+                t[1] = make_int4(0, 0, 0, 0);
             }
         }
     }
@@ -301,7 +304,10 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                 uint8_t* dst = slot_of(a, prb, d, sh);
                 if (dst) {
                     bulk_store(dst, q, static_cast<uint32_t>(a.H));
-                    *reinterpret_cast<float*>(dst + a.scale_off) = scale;
+                    // Scale plus zero padding: one whole 32-byte sector.
+                    int4* sc = reinterpret_cast<int4*>(dst + a.scale_off);
+                    sc[0] = make_int4(__float_as_int(scale), 0, 0, 0);
+                    sc[1] = make_int4(0, 0, 0, 0);
                 }
             }
         }

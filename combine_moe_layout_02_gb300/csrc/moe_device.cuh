@@ -189,6 +189,10 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const moe_shape& s, CombineArgs a, cudaStream_t stream);
 
+cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* prb, uint8_t* arena,
+                       int64_t arena_rows, int32_t* src_idx, int32_t* tk_idx, float* tk_w,
+                       cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -25,7 +25,7 @@ MOE_ERR_INCONSISTENT = 7
 
 EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
-           "moe_layout_static_scratch")
+           "moe_layout_static_scratch", "moe_pad_partitions")
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
 MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_combine.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+    L.moe_pad_partitions.restype = i32
+    L.moe_pad_partitions.argtypes = [sp, vp, vp, vp, i64, vp, vp, vp, vp]
     L.moe_layout_static_scratch.restype = i32
     L.moe_layout_static_scratch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
     _lib = L
@@ -179,6 +181,14 @@ def moe_combine(shape, y, y_row_stride, part_row_base, arena_rows, send_head, to
     _check(st, "moe_combine")
 
 
+def moe_pad_partitions(shape, num_recv_tokens, part_row_base, recv_arena, arena_rows,
+                       recv_src_idx, recv_topk_idx, recv_topk_weights, stream=None):
+    st = lib().moe_pad_partitions(ctypes.byref(shape), _ptr(num_recv_tokens), _ptr(part_row_base),
+                                  _ptr(recv_arena), int(arena_rows), _ptr(recv_src_idx),
+                                  _ptr(recv_topk_idx), _ptr(recv_topk_weights), _stream(stream))
+    _check(st, "moe_pad_partitions")
+
+
 def moe_layout_static_scratch(shape, topk_idx, num_tokens_per_rank, num_tokens_per_expert,
                               is_token_in_rank, is_token_in_rank_bits, err, stream=None):
     """moe_layout using the library's built-in scratch buffer: for callers that
@@ -254,6 +264,12 @@ class Buffers:
             y, y_row_stride = self.recv_arena, self.stride
         moe_combine(self.shape, y, y_row_stride, self.part_row_base, self.arena_rows, self.send_head,
                     topk_idx, topk_weights, out, self.err, stream)
+
+    def pad(self, stream=None):
+        """Pad fixed-capacity partitions past their received counts."""
+        moe_pad_partitions(self.shape, self.num_recv_tokens, self.part_row_base, self.recv_arena,
+                           self.arena_rows, self.recv_src_idx, self.recv_topk_idx,
+                           self.recv_topk_weights, stream)
 
     def step(self, x, topk_idx, topk_weights, out, stream=None):
         """One pass of the hot path: layout -> notify -> dispatch -> combine."""

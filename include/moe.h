@@ -93,9 +93,10 @@ moe_status moe_check_shape(const moe_shape* shape);
  * section 2.3 token format and section 8.2 size check):
  *   Ceil(Ceil(H * elt, 32) + 44, 512), elt = 2 (bf16) or 1 (int8).
  * Slot layout: payload [0, H*elt); fp32 scale at byte Ceil(H*elt, 32)
- * (int8 only); int32 triple (source rank, source-local token, lowest k whose
- * expert is on this rank) at byte Ceil(H*elt, 32) + 32 (16 bytes written, the
- * last 4 are zero); the rest is padding and is not written.
+ * (int8 only; its 32-byte block is written, zero after the scale); int32
+ * triple (source rank, source-local token, lowest k whose expert is on this
+ * rank) at byte Ceil(H*elt, 32) + 32 (its 32-byte block is written, zero
+ * after the triple); the rest is padding and is not written.
  * 14848 bytes for H = 7168 bf16. Returns -1 for H < 1. */
 int64_t moe_slot_stride(int32_t H, int32_t quant);
 
@@ -221,6 +222,28 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
                        const int64_t* part_row_base, int64_t arena_rows,
                        const int32_t* send_head, const int32_t* topk_idx,
                        const float* topk_weights, uint16_t* out, int32_t* err, void* stream);
+
+/*
+ * moe_pad_partitions -- fixed-length receive partitions ("Ascend DeepEP MoE
+ * Dispatch Optimization", section "输出长度有动态和固定两种模式": with a fixed
+ * output length, num_worst_tokens, the host reads no count back and the rows
+ * past the received count are padding -- x, scales and weights 0, topk_idx -1).
+ *
+ * With fixed-capacity partitions (part_row_base[d] = d * capacity, passed to
+ * moe_dispatch) this fills, for every rank d, the rows from
+ * part_row_base[d] + num_recv_tokens[d] up to part_row_base[d+1] (and below
+ * arena_rows): payload 0, the scale block 0 (int8 slots), the triple
+ * (-1, -1, -1), recv_src_idx -1, recv_topk_idx -1, recv_topk_weights 0 (each
+ * side array may be NULL). A partition that overflowed (count > capacity) has
+ * no padding; moe_dispatch reports the overflow rather than truncating.
+ *
+ *   num_recv_tokens int32 [P] (from moe_notify); part_row_base int64 [P+1];
+ *   recv_arena / side arrays as for moe_dispatch. Only padding rows are written.
+ */
+moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_tokens,
+                              const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,
+                              int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                              void* stream);
 
 /*
  * moe_layout_static_scratch -- moe_layout without a caller-provided scratch

@@ -63,6 +63,8 @@ def _load():
     lib.oracle_combine.restype = i32
     lib.oracle_combine.argtypes = [i32, i32, i64, i32, i32, vp, i64, vp, i64, vp, vp,
                                    vp, vp, vp, i64]
+    lib.oracle_pad_partitions.restype = None
+    lib.oracle_pad_partitions.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp]
     lib.oracle_bf16_round.restype = None
     lib.oracle_bf16_round.argtypes = [vp, vp, i64]
     _lib = lib
@@ -182,6 +184,20 @@ def combine(P: int, E: int, H: int, y: np.ndarray, y_row_stride: int, part_row_b
                                  _p(send_head), _p(topk_idx), _p(w), _p(out),
                                  _p(tok), 0 if tok is None else int(tok.shape[0]))
     return dict(out=out, err=int(err))
+
+
+def pad_partitions(P: int, K: int, H: int, quant: int, num_recv_tokens: np.ndarray,
+                   part_row_base: np.ndarray, arena: np.ndarray, recv_src_idx=None,
+                   recv_topk_idx=None, recv_topk_weights=None) -> None:
+    """Fill the padding rows of fixed-length partitions in place."""
+    nrt = _c(num_recv_tokens, np.int32)
+    prb = _c(part_row_base, np.int64)
+    assert arena.flags.c_contiguous and arena.dtype == np.uint8
+    rows = arena.shape[0]
+    for a, dt in ((recv_src_idx, np.int32), (recv_topk_idx, np.int32), (recv_topk_weights, np.float32)):
+        assert a is None or (a.flags.c_contiguous and a.dtype == dt)
+    _load().oracle_pad_partitions(P, K, H, quant, _p(nrt), _p(prb), _p(arena), int(rows),
+                                  _p(recv_src_idx), _p(recv_topk_idx), _p(recv_topk_weights))
 
 
 def bf16_round(values: np.ndarray) -> np.ndarray:

@@ -345,6 +345,38 @@ int32_t oracle_combine(int32_t P, int32_t E, int64_t S, int32_t K, int32_t H,
     return err;
 }
 
+// Fixed-length receive partitions ("Ascend DeepEP MoE Dispatch Optimization",
+// section "输出长度有动态和固定两种模式": with a fixed output length the rows
+// past the received count are padding -- x, scales and weights 0, topk_idx
+// -1). For every rank d the rows part_row_base[d] + num_recv_tokens[d] up to
+// part_row_base[d+1] (and below arena_rows) get: payload 0; the scale block 0
+// (int8); the triple (-1, -1, -1); recv_src_idx -1; recv_topk_idx -1;
+// recv_topk_weights 0.
+void oracle_pad_partitions(int32_t P, int32_t K, int32_t H, int32_t quant,
+                           const int32_t* num_recv_tokens, const int64_t* part_row_base,
+                           uint8_t* arena, int64_t arena_rows, int32_t* recv_src_idx,
+                           int32_t* recv_topk_idx, float* recv_topk_weights) {
+    const int64_t stride = oracle_slot_stride(H, quant);
+    const int64_t elt = quant ? 1 : 2;
+    const int64_t scale_off = ceil_to(static_cast<int64_t>(H) * elt, 32);
+    const int64_t triple_off = scale_off + 32;
+    for (int32_t d = 0; d < P; ++d) {
+        for (int64_t r = part_row_base[d] + num_recv_tokens[d]; r < part_row_base[d + 1]; ++r) {
+            if (r < 0 || r >= arena_rows) continue;
+            uint8_t* slot = arena + r * stride;
+            std::memset(slot, 0, static_cast<size_t>(H) * elt);
+            if (quant) std::memset(slot + scale_off, 0, 32);
+            const int32_t triple[3] = {-1, -1, -1};
+            std::memcpy(slot + triple_off, triple, 12);
+            if (recv_src_idx) recv_src_idx[r] = -1;
+            for (int32_t k = 0; k < K; ++k) {
+                if (recv_topk_idx) recv_topk_idx[r * K + k] = -1;
+                if (recv_topk_weights) recv_topk_weights[r * K + k] = 0.0f;
+            }
+        }
+    }
+}
+
 // Exposed for the pin tests of the conversion helpers.
 void oracle_bf16_round(const float* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16_bits_rne(in[i]);

@@ -198,3 +198,60 @@ def test_full_size_sampled(name, quant, y_mode):
         masked_any = (w.topk_idx < 0).any()
         if not masked_any:
             assert d.max() <= 1
+
+
+def test_cached_dispatch_reuses_the_handle():
+    """Same routing, new hidden rows: dispatch with the handle of the first
+    pass (no layout / notify) equals a fresh dispatch of the new rows."""
+    import torch
+
+    w = inputs.workload("p32_e256_t128_h1024", T=33)
+    gpu = gp.run_gpu(w)
+    buf = gpu["buf"]
+    lay, nt = gp.oracle_tables(w)
+    w2 = inputs.workload("p32_e256_t128_h1024", T=33, seed=5)   # same shape, new x (and routing)
+    w.x_bits = w2.x_bits
+    x2 = torch.from_numpy(w.x_bits.view(np.int16)).cuda()
+    idx = torch.from_numpy(w.topk_idx).cuda()
+    wts = torch.from_numpy(w.topk_weights).cuda()
+    buf.recv_arena.zero_()
+    buf.dispatch(x2, idx, wts)
+    out = torch.empty((w.S, w.H), dtype=torch.int16, device="cuda")
+    buf.combine(out, idx, wts)
+    torch.cuda.synchronize()
+    assert int(buf.err[0].item()) == 0
+    gp.compare_dispatch(w, 0, gpu, nt)
+    gpu["out"] = out.cpu().numpy().view(np.uint16)
+    gp.compare_combine(w, gpu, nt)
+
+
+@pytest.mark.parametrize("quant", [0, 1])
+def test_fixed_capacity_with_padding(quant):
+    """num_worst_tokens form: fixed partitions, padding rows filled by
+    moe_pad_partitions exactly as the oracle fills them."""
+    import torch
+    import oracle
+
+    w = inputs.make(4, 16, 100, 256, 3, seed=12, mask_frac=0.2)
+    lay, nt = gp.oracle_tables(w)
+    cap = int(nt["num_recv_tokens"].max()) + 7
+    prb = np.arange(w.P + 1, dtype=np.int64) * cap
+    gpu = gp.run_gpu(w, quant=quant, arena_rows=cap * w.P, part_row_base=prb,
+                     y_mode="int8expert" if quant else "identity")
+    buf = gpu["buf"]
+    buf.pad()
+    torch.cuda.synchronize()
+    ref = oracle.dispatch(w.P, w.E, w.H, quant, w.x_bits, w.topk_idx, w.topk_weights,
+                          nt["send_head"], prb, cap * w.P)
+    oracle.pad_partitions(w.P, w.K, w.H, quant, nt["num_recv_tokens"], prb, ref["arena"],
+                          ref["recv_src_idx"], ref["recv_topk_idx"], ref["recv_topk_weights"])
+    pay, scale_off, triple_off = gp.offsets(w.H, quant)
+    g_arena = buf.recv_arena.cpu().numpy()
+    np.testing.assert_array_equal(g_arena[:, :pay], ref["arena"][:, :pay])
+    np.testing.assert_array_equal(g_arena[:, triple_off:triple_off + 12],
+                                  ref["arena"][:, triple_off:triple_off + 12])
+    if quant:
+        np.testing.assert_array_equal(g_arena[:, scale_off:scale_off + 4],
+                                      ref["arena"][:, scale_off:scale_off + 4])
+    for k in ("recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        np.testing.assert_array_equal(getattr(buf, k).cpu().numpy(), ref[k], err_msg=k)

@@ -142,3 +142,49 @@ def test_token_subset_writes_only_those_rows():
     np.testing.assert_array_equal(sub["arena"][written], full["arena"][written])
     others = np.setdiff1d(np.arange(rows), written)
     assert (sub["arena"][others] == 0).all()
+
+
+def _worst_tokens_case():
+    """P=2 ranks, capacity 256 rows each; rank 0 receives 237 rows (the page's
+    example), rank 1 receives 200."""
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "worst_tokens.json")) as f:
+        gold = json.load(f)
+    P, E, K, H, T = 2, 4, 1, 64, 256
+    idx = np.full((P * T, K), -1, np.int32)
+    idx[:gold["received"], 0] = np.arange(gold["received"]) % 2          # experts 0/1 -> rank 0
+    idx[gold["received"]:gold["received"] + 200, 0] = 2                  # expert 2 -> rank 1
+    rng = np.random.default_rng(0)
+    x = (rng.integers(0, 1 << 15, size=(P * T, H)) | 0x3C00).astype(np.uint16)
+    w = np.ones((P * T, K), np.float32)
+    return gold, P, E, K, H, T, idx, x, w
+
+
+def test_worst_tokens_padding_matches_page_example():
+    gold, P, E, K, H, T, idx, x, w = _worst_tokens_case()
+    cap = gold["capacity"]
+    lay = oracle.layout(P, E, idx)
+    nt = oracle.notify(P, E, 4, 1, lay["num_tokens_per_rank"], lay["num_tokens_per_expert"],
+                       lay["is_token_in_rank"])
+    assert nt["num_recv_tokens"].tolist() == [gold["received"], 200]
+    prb = np.arange(P + 1, dtype=np.int64) * cap
+    dis = oracle.dispatch(P, E, H, 0, x, idx, w, nt["send_head"], prb, P * cap)
+    assert dis["err"] == 0
+    oracle.pad_partitions(P, K, H, 0, nt["num_recv_tokens"], prb, dis["arena"], dis["recv_src_idx"],
+                          dis["recv_topk_idx"], dis["recv_topk_weights"])
+    _, triple_off = _offsets(H, 0)
+    pad = np.arange(gold["received"], cap)
+    assert pad.shape[0] == gold["padding_rows"]
+    assert (dis["arena"][pad, :2 * H] == 0).all()                       # x = 0
+    assert (dis["recv_topk_weights"][pad] == 0).all()                   # weights = 0
+    assert (dis["recv_topk_idx"][pad] == -1).all()                      # topk_idx = -1
+    assert (dis["recv_src_idx"][pad] == -1).all()
+    assert (dis["arena"][pad, triple_off:triple_off + 12].view(np.int32) == -1).all()
+    # The 237 valid rows are untouched by the padding: row r holds token r's x.
+    for r in range(gold["received"]):
+        np.testing.assert_array_equal(dis["arena"][r, :2 * H].view(np.uint16), x[r])
+    # Rank 1: 200 valid rows, 56 padding rows.
+    assert (dis["recv_topk_idx"][cap + 200:2 * cap] == -1).all()
+    assert (dis["recv_topk_idx"][cap:cap + 200] == 0).all()
