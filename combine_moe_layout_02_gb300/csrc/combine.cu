@@ -72,6 +72,7 @@ __device__ __forceinline__ TokenRoute load_route(const CombineArgs& a, int64_t g
 
 template <int MAXR>
 __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_kernel(const CombineArgs a) {
+    pdl_wait_then_release();
     extern __shared__ __align__(16) int64_t prb[];  // [P+1]
     const int tid = threadIdx.x, lane = tid & 31;
     for (int i = tid; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
@@ -184,8 +185,7 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int64_t needed = ceil_div(a.S, warps_per_block);
     if (grid > needed) grid = needed;
-    combine_kernel<MAXR><<<static_cast<unsigned>(grid), kCombineThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<MAXR>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a);
 }
 
 }  // namespace

@@ -136,6 +136,7 @@ __device__ void drain_loads(uint64_t* bars, int stages, int64_t first, int64_t l
 }
 
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchArgs a) {
+    pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, false);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
@@ -225,6 +226,7 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float scale, bool zer
 }
 
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
+    pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[kInt8Threads / 32];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, true);
@@ -348,11 +350,8 @@ cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t str
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
     if (grid > a.S) grid = a.S;
-    if (quant)
-        dispatch_int8_kernel<<<static_cast<unsigned>(grid), threads, L.total, stream>>>(a);
-    else
-        dispatch_bf16_kernel<<<static_cast<unsigned>(grid), threads, L.total, stream>>>(a);
-    return cudaGetLastError();
+    if (quant) return launch_pdl(dispatch_int8_kernel, static_cast<unsigned>(grid), threads, L.total, stream, a);
+    return launch_pdl(dispatch_bf16_kernel, static_cast<unsigned>(grid), threads, L.total, stream, a);
 }
 
 }  // namespace moe

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kLayoutMaxThreads)
 layout_count_kernel(int32_t P, int32_t E, int32_t K, int64_t T, int64_t nbs, int64_t part_stride,
                     const int32_t* __restrict__ topk_idx, uint8_t* __restrict__ itr,
                     uint32_t* __restrict__ bits, int32_t* __restrict__ part) {
+    pdl_wait_then_release();
     extern __shared__ __align__(16) unsigned char smem[];
     const int tb = blockDim.x;
     const int nwarps = tb >> 5;
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(kReduceThreads)
 layout_reduce_kernel(int32_t P, int32_t E, int64_t nbs, int64_t part_stride,
                      const int32_t* __restrict__ part, int32_t* __restrict__ ntpr,
                      int32_t* __restrict__ ntpe, int32_t* __restrict__ err) {
+    pdl_wait_then_release();
     const int64_t s = blockIdx.x;
     const int32_t* base = part + s * nbs * part_stride;
     for (int j = threadIdx.x; j < P + E; j += blockDim.x) {
@@ -175,17 +177,19 @@ cudaError_t launch_layout(const moe_shape& s, const int32_t* topk_idx, int32_t* 
     const LayoutPlan p = layout_plan(s);
     int32_t* part = static_cast<int32_t*>(scratch);
     const int64_t blocks = static_cast<int64_t>(s.P) * p.blocks_per_source;
+    cudaError_t e = cudaSuccess;
     if (blocks > 0) {
-        cudaError_t e = cudaFuncSetAttribute(layout_count_kernel,
+        e = cudaFuncSetAttribute(layout_count_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(p.smem));
         if (e != cudaSuccess) return e;
-        layout_count_kernel<<<static_cast<unsigned>(blocks), p.threads, p.smem, stream>>>(
-            s.P, s.E, s.K, s.S / s.P, p.blocks_per_source, p.part_stride, topk_idx, itr, bits, part);
+        e = launch_pdl(layout_count_kernel, static_cast<unsigned>(blocks), p.threads, p.smem, stream, s.P,
+                       s.E, s.K, static_cast<int64_t>(s.S / s.P), p.blocks_per_source, p.part_stride,
+                       topk_idx, itr, bits, part);
+        if (e != cudaSuccess) return e;
     }
-    layout_reduce_kernel<<<s.P, kReduceThreads, 0, stream>>>(s.P, s.E, p.blocks_per_source,
-                                                             p.part_stride, part, ntpr, ntpe, err);
-    return cudaGetLastError();
+    return launch_pdl(layout_reduce_kernel, static_cast<unsigned>(s.P), kReduceThreads, 0, stream, s.P, s.E,
+                      p.blocks_per_source, p.part_stride, static_cast<const int32_t*>(part), ntpr, ntpe, err);
 }
 
 }  // namespace moe

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -106,6 +108,16 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
     return v;
 }
 
+// Programmatic dependent launch. Every kernel of the path is launched with
+// programmatic stream serialisation: it may be scheduled while the previous
+// kernel on the stream is still running. It waits for that kernel (and so,
+// transitively, everything before it) to complete and flush before its first
+// global-memory access, then lets the next kernel be scheduled.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -195,5 +207,24 @@ cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* pr
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Launch `kernel` on `stream` with programmatic stream serialisation (see
+// pdl_wait_then_release); the kernel must call pdl_wait_then_release before
+// touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace moe

@@ -10,23 +10,64 @@
 // rank is the c-th block of the balanced split of "HCCL Window 模式
 // (Non-SHMEM) 代码深度剖析", section 8.3.
 //
-// Two launches, both one block per (source rank, channel):
-//  1. notify_count_kernel: per-rank counts of the channel's tokens (warp
-//     ballots into per-warp shared counters, fixed-order block sum) into
-//     scratch. One extra block computes the rank prefix matrix, receive
-//     totals, packed partition bases and the per-expert counts and offsets.
-//  2. notify_head_kernel: channel prefixes from the scratch counts, then
-//     send_head for the channel's tokens: ballot + popc of the lanes below
-//     (rank inside the warp), an exclusive scan over the block's warps and a
-//     running carry across block-sized chunks.
+// Two launches. Work is handed out per warp, so every block shape works:
+//  1. notify_count_kernel
+//     - channel part: per-rank token counts of each (source rank, channel)
+//       into scratch;
+//     - rank part: one warp per destination column scans num_tokens_per_rank
+//       down the source ranks (warp-shuffle scan with a carry) into
+//       rank_prefix_matrix and num_recv_tokens;
+//     - expert part: one warp per expert sums num_tokens_per_expert over
+//       source ranks and rounds up to expert_alignment.
+//  2. notify_head_kernel
+//     - channel part: channel prefixes from the scratch counts, then
+//       send_head for the channel's tokens;
+//     - tail part: one warp per rank scans its per-expert counts into
+//       recv_expert_offset; warp 0 scans the receive totals into the packed
+//       partition bases.
+// The channel part has two shapes:
+//   * token-major (P < 32 or P % 4 != 0): one block per channel, one thread
+//     per token; per rank a __ballot_sync, __popc of the lower lanes for the
+//     rank inside the warp, and a scan over the block's warps;
+//   * rank-major (P >= 32, P % 4 == 0): one warp per channel, each lane owns 4
+//     ranks and walks the channel's tokens in order with 4 running counters;
+//     a token's send_head row is one coalesced 16-byte store per lane.
 // No atomics: every output is a fixed-order integer sum.
 #include "moe_device.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kNotifyThreads = 256;
-constexpr int kNotifyWarps = kNotifyThreads / 32;
+constexpr int kMaxThreads = 256;
+
+struct NotifyPlan {
+    bool rank_major;
+    int threads;             // block size
+    int wpb;                 // warps per block
+    int64_t chan_blocks;     // blocks of the channel part
+    int64_t rank_blocks;     // kernel 1: rank-prefix blocks
+    int64_t expert_blocks;   // kernel 1: expert-sum blocks
+    int64_t tail_blocks;     // kernel 2: offset / base blocks
+};
+
+NotifyPlan notify_plan(const moe_shape& s) {
+    NotifyPlan p;
+    const int64_t T = s.S / s.P;
+    const int64_t chans = static_cast<int64_t>(s.P) * s.num_channels;
+    p.rank_major = s.P >= 32 && (s.P % 4) == 0;
+    if (p.rank_major) {
+        p.threads = kMaxThreads;
+    } else {
+        int64_t t = round_up(ceil_div(T, s.num_channels), 32);
+        p.threads = static_cast<int>(t < 32 ? 32 : (t > kMaxThreads ? kMaxThreads : t));
+    }
+    p.wpb = p.threads / 32;
+    p.chan_blocks = p.rank_major ? ceil_div(chans, p.wpb) : chans;
+    p.rank_blocks = ceil_div(s.P, p.wpb);
+    p.expert_blocks = ceil_div(s.E, p.wpb);
+    p.tail_blocks = ceil_div(s.P, p.wpb);
+    return p;
+}
 
 // For each rank d, ballot "token of this lane is bound for d" over the warp and
 // hand the ballot to f(d, ballot). Loads the token's row 4 bytes at a time
@@ -50,80 +91,87 @@ __device__ __forceinline__ void for_each_rank_ballot(const uint8_t* row, bool ac
     }
 }
 
-// The extra block of notify_count_kernel: everything that only depends on the
-// per-source count matrices.
-__device__ void notify_prefix_block(int32_t P, int32_t E, int32_t A, const int32_t* __restrict__ ntpr,
-                                    const int32_t* __restrict__ ntpe, int32_t* __restrict__ rpm,
-                                    int32_t* __restrict__ nrt, int32_t* __restrict__ nrtpe,
-                                    int32_t* __restrict__ reo, int64_t* __restrict__ part_row_base,
-                                    int32_t* tot /* shared, [P] */) {
-    __shared__ int64_t warp_sum[kNotifyWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int epr = E / P;
-    for (int d = tid; d < P; d += nthreads) {
-        int32_t run = 0;
-#pragma unroll 8
-        for (int s = 0; s < P; ++s) {
-            run += ntpr[s * P + d];
-            rpm[s * P + d] = run;
-        }
-        nrt[d] = run;
-        tot[d] = run;
-    }
-    for (int e = tid; e < E; e += nthreads) {
-        int64_t cnt = 0;
-#pragma unroll 8
-        for (int s = 0; s < P; ++s) cnt += ntpe[static_cast<int64_t>(s) * E + e];
-        nrtpe[e] = static_cast<int32_t>(round_up(cnt, A));
-    }
-    __syncthreads();
-    // Packed partition bases: exclusive scan of the receive totals.
-    const int per = static_cast<int>(ceil_div(P, nthreads));
-    const int d0 = min(P, tid * per), d1 = min(P, d0 + per);
-    int64_t local = 0;
-    for (int d = d0; d < d1; ++d) local += tot[d];
-    int64_t incl = local;
+template <typename V>
+__device__ __forceinline__ V warp_inclusive_scan(V v, int lane) {
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const V u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
     }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    int64_t before = 0;
-    for (int w = 0; w < warp; ++w) before += warp_sum[w];
-    int64_t run = before + incl - local;
-    for (int d = d0; d < d1; ++d) {
-        part_row_base[d] = run;
-        run += tot[d];
-    }
-    if (d0 < d1 && d1 == P) part_row_base[P] = run;
-    // Per-expert offsets inside each rank.
-    for (int d = tid; d < P; d += nthreads) {
-        int32_t off = 0;
-        for (int l = 0; l < epr; ++l) {
-            reo[d * epr + l] = off;
-            off += nrtpe[d * epr + l];
-        }
-    }
+    return v;
 }
 
-__global__ void __launch_bounds__(kNotifyThreads)
-notify_count_kernel(int32_t P, int32_t E, int32_t C, int32_t A, int64_t T,
-                    const int32_t* __restrict__ ntpr, const int32_t* __restrict__ ntpe,
-                    const uint8_t* __restrict__ itr, int32_t* __restrict__ rpm,
-                    int32_t* __restrict__ nrt, int32_t* __restrict__ nrtpe, int32_t* __restrict__ reo,
-                    int64_t* __restrict__ part_row_base, int32_t* __restrict__ ccount) {
-    extern __shared__ __align__(16) int32_t wcnt[];  // [warps][P]
+__device__ __forceinline__ int flag(uint32_t w, int j) { return ((w >> (8 * j)) & 0xffu) != 0u; }
+
+// ---- kernel 1 -------------------------------------------------------------
+
+__global__ void __launch_bounds__(kMaxThreads)
+notify_count_kernel(int32_t P, int32_t E, int32_t C, int32_t A, int64_t T, bool rank_major,
+                    int64_t chan_blocks, int64_t rank_blocks, const int32_t* __restrict__ ntpr,
+                    const int32_t* __restrict__ ntpe, const uint8_t* __restrict__ itr,
+                    int32_t* __restrict__ rpm, int32_t* __restrict__ nrt, int32_t* __restrict__ nrtpe,
+                    int32_t* __restrict__ ccount) {
+    pdl_wait_then_release();
+    extern __shared__ __align__(16) int32_t wcnt[];  // token-major: [warps][P]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int nwarps = nthreads >> 5;
-    if (blockIdx.x == static_cast<unsigned>(P) * C) {
-        notify_prefix_block(P, E, A, ntpr, ntpe, rpm, nrt, nrtpe, reo, part_row_base, wcnt);
+    const int wpb = nthreads >> 5;
+    const int64_t bid = blockIdx.x;
+
+    if (bid >= chan_blocks) {
+        if (bid < chan_blocks + rank_blocks) {
+            // Rank part: column d of num_tokens_per_rank, scanned over sources.
+            const int64_t gw = (bid - chan_blocks) * wpb + warp;
+            if (gw >= P) return;
+            const int d = static_cast<int>(gw);
+            int32_t carry = 0;
+            for (int s0 = 0; s0 < P; s0 += 32) {
+                const int s = s0 + lane;
+                const int32_t v = s < P ? __ldg(ntpr + static_cast<int64_t>(s) * P + d) : 0;
+                const int32_t incl = warp_inclusive_scan(v, lane);
+                if (s < P) rpm[static_cast<int64_t>(s) * P + d] = carry + incl;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) nrt[d] = carry;
+        } else {
+            // Expert part: receive count of expert e, summed over sources, aligned.
+            const int64_t gw = (bid - chan_blocks - rank_blocks) * wpb + warp;
+            if (gw >= E) return;
+            int64_t sum = 0;
+            for (int s = lane; s < P; s += 32) sum += __ldg(ntpe + static_cast<int64_t>(s) * E + gw);
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) nrtpe[gw] = static_cast<int32_t>(round_up(sum, A));
+        }
         return;
     }
-    const int64_t s = blockIdx.x / C, c = blockIdx.x % C;
+
+    if (rank_major) {
+        const int64_t ch = bid * wpb + warp;
+        if (ch >= static_cast<int64_t>(P) * C) return;
+        const int64_t s = ch / C, c = ch % C;
+        int64_t b, e;
+        split_range(T, C, c, &b, &e);
+        for (int d0 = 0; d0 < P; d0 += 128) {
+            const int d = d0 + 4 * lane;
+            if (d >= P) continue;
+            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll 4
+            for (int64_t t = b; t < e; ++t) {
+                const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + (s * T + t) * P + d));
+                c0 += flag(w, 0);
+                c1 += flag(w, 1);
+                c2 += flag(w, 2);
+                c3 += flag(w, 3);
+            }
+            *reinterpret_cast<int4*>(ccount + ch * P + d) = make_int4(c0, c1, c2, c3);
+        }
+        return;
+    }
+
+    // Token-major channel counts.
+    const int64_t s = bid / C, c = bid % C;
     int64_t b, e;
     split_range(T, C, c, &b, &e);
-    for (int i = tid; i < nwarps * P; i += nthreads) wcnt[i] = 0;
+    for (int i = tid; i < wpb * P; i += nthreads) wcnt[i] = 0;
     __syncthreads();
     int32_t* mine = wcnt + warp * P;
     for (int64_t t0 = b; t0 < e; t0 += nthreads) {
@@ -137,22 +185,102 @@ notify_count_kernel(int32_t P, int32_t E, int32_t C, int32_t A, int64_t T,
     __syncthreads();
     for (int d = tid; d < P; d += nthreads) {
         int32_t sum = 0;
-        for (int w = 0; w < nwarps; ++w) sum += wcnt[w * P + d];
-        ccount[static_cast<int64_t>(blockIdx.x) * P + d] = sum;
+        for (int w = 0; w < wpb; ++w) sum += wcnt[w * P + d];
+        ccount[bid * P + d] = sum;
     }
 }
 
-__global__ void __launch_bounds__(kNotifyThreads)
-notify_head_kernel(int32_t P, int32_t C, int64_t T, const uint8_t* __restrict__ itr,
-                   const int32_t* __restrict__ rpm, const int32_t* __restrict__ ccount,
-                   int32_t* __restrict__ cpm, int32_t* __restrict__ rcpm,
-                   int32_t* __restrict__ send_head) {
+// ---- kernel 2 -------------------------------------------------------------
+
+__global__ void __launch_bounds__(kMaxThreads)
+notify_head_kernel(int32_t P, int32_t E, int32_t C, int64_t T, bool rank_major, int64_t chan_blocks,
+                   const uint8_t* __restrict__ itr, const int32_t* __restrict__ rpm,
+                   const int32_t* __restrict__ nrt, const int32_t* __restrict__ nrtpe,
+                   const int32_t* __restrict__ ccount, int32_t* __restrict__ cpm,
+                   int32_t* __restrict__ rcpm, int32_t* __restrict__ send_head,
+                   int32_t* __restrict__ reo, int64_t* __restrict__ part_row_base) {
+    pdl_wait_then_release();
     extern __shared__ __align__(16) int32_t sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int nwarps = nthreads >> 5;
-    int32_t* base = sm;           // [P]   next free row of d for this channel
-    int32_t* woff = sm + P;       // [warps][P]
-    const int64_t s = blockIdx.x / C, c = blockIdx.x % C;
+    const int wpb = nthreads >> 5;
+    const int64_t bid = blockIdx.x;
+
+    if (bid >= chan_blocks) {
+        // Tail part: per-rank expert offsets; warp 0 also the partition bases.
+        const int64_t gw = (bid - chan_blocks) * wpb + warp;
+        if (gw >= P) return;
+        const int epr = E / P;
+        const int64_t d = gw;
+        int32_t carry = 0;
+        for (int l0 = 0; l0 < epr; l0 += 32) {
+            const int l = l0 + lane;
+            const int32_t v = l < epr ? __ldg(nrtpe + d * epr + l) : 0;
+            const int32_t incl = warp_inclusive_scan(v, lane);
+            if (l < epr) reo[d * epr + l] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (gw == 0) {
+            int64_t run = 0;
+            for (int d0 = 0; d0 < P; d0 += 32) {
+                const int dd = d0 + lane;
+                const int64_t v = dd < P ? __ldg(nrt + dd) : 0;
+                const int64_t incl = warp_inclusive_scan(v, lane);
+                if (dd < P) part_row_base[dd] = run + incl - v;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) part_row_base[P] = run;
+        }
+        return;
+    }
+
+    if (rank_major) {
+        const int64_t ch = bid * wpb + warp;
+        if (ch >= static_cast<int64_t>(P) * C) return;
+        const int64_t s = ch / C, c = ch % C;
+        int64_t b, e;
+        split_range(T, C, c, &b, &e);
+        for (int d0 = 0; d0 < P; d0 += 128) {
+            const int d = d0 + 4 * lane;
+            if (d >= P) continue;
+            int4 pre = make_int4(0, 0, 0, 0);
+            for (int64_t cc = 0; cc < c; ++cc) {
+                const int4 v = __ldg(reinterpret_cast<const int4*>(ccount + (s * C + cc) * P + d));
+                pre.x += v.x;
+                pre.y += v.y;
+                pre.z += v.z;
+                pre.w += v.w;
+            }
+            const int4 cnt = __ldg(reinterpret_cast<const int4*>(ccount + ch * P + d));
+            const int4 rb = s > 0 ? __ldg(reinterpret_cast<const int4*>(rpm + (s - 1) * P + d))
+                                  : make_int4(0, 0, 0, 0);
+            cpm[(s * P + d + 0) * C + c] = pre.x + cnt.x;
+            cpm[(s * P + d + 1) * C + c] = pre.y + cnt.y;
+            cpm[(s * P + d + 2) * C + c] = pre.z + cnt.z;
+            cpm[(s * P + d + 3) * C + c] = pre.w + cnt.w;
+            int32_t b0 = rb.x + pre.x, b1 = rb.y + pre.y, b2 = rb.z + pre.z, b3 = rb.w + pre.w;
+            rcpm[(static_cast<int64_t>(d + 0) * P + s) * C + c] = b0;
+            rcpm[(static_cast<int64_t>(d + 1) * P + s) * C + c] = b1;
+            rcpm[(static_cast<int64_t>(d + 2) * P + s) * C + c] = b2;
+            rcpm[(static_cast<int64_t>(d + 3) * P + s) * C + c] = b3;
+#pragma unroll 4
+            for (int64_t t = b; t < e; ++t) {
+                const int64_t g = s * T + t;
+                const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + g * P + d));
+                int4 v;
+                v.x = flag(w, 0) ? b0++ : -1;
+                v.y = flag(w, 1) ? b1++ : -1;
+                v.z = flag(w, 2) ? b2++ : -1;
+                v.w = flag(w, 3) ? b3++ : -1;
+                *reinterpret_cast<int4*>(send_head + g * P + d) = v;
+            }
+        }
+        return;
+    }
+
+    // Token-major channel heads.
+    int32_t* base = sm;      // [P]   next free row of d for this channel
+    int32_t* woff = sm + P;  // [warps][P]
+    const int64_t s = bid / C, c = bid % C;
     int64_t b, e;
     split_range(T, C, c, &b, &e);
     for (int d = tid; d < P; d += nthreads) {
@@ -178,7 +306,7 @@ notify_head_kernel(int32_t P, int32_t C, int64_t T, const uint8_t* __restrict__ 
         __syncthreads();
         for (int d = tid; d < P; d += nthreads) {
             int32_t run = base[d];
-            for (int w = 0; w < nwarps; ++w) {
+            for (int w = 0; w < wpb; ++w) {
                 const int32_t cnt = woff[w * P + d];
                 woff[w * P + d] = run;
                 run += cnt;
@@ -223,22 +351,26 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
                           int32_t* nrt, int32_t* nrtpe, int32_t* reo, int32_t* send_head,
                           int64_t* part_row_base, void* scratch, cudaStream_t stream) {
     const int64_t T = s.S / s.P;
+    const NotifyPlan p = notify_plan(s);
     int32_t* ccount = static_cast<int32_t*>(scratch);
-    const int64_t chans = static_cast<int64_t>(s.P) * s.num_channels;
-    const size_t smem_count = static_cast<size_t>(kNotifyWarps) * s.P * 4;
-    const size_t smem_head = static_cast<size_t>(kNotifyWarps + 1) * s.P * 4;
+    const size_t smem_count = p.rank_major ? 0 : static_cast<size_t>(p.wpb) * s.P * 4;
+    const size_t smem_head = p.rank_major ? 0 : static_cast<size_t>(p.wpb + 1) * s.P * 4;
     cudaError_t e = cudaFuncSetAttribute(notify_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_count));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(notify_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_head));
     if (e != cudaSuccess) return e;
-    notify_count_kernel<<<static_cast<unsigned>(chans + 1), kNotifyThreads, smem_count, stream>>>(
-        s.P, s.E, s.num_channels, s.expert_alignment, T, ntpr, ntpe, itr, rpm, nrt, nrtpe, reo,
-        part_row_base, ccount);
-    notify_head_kernel<<<static_cast<unsigned>(chans), kNotifyThreads, smem_head, stream>>>(
-        s.P, s.num_channels, T, itr, rpm, ccount, cpm, rcpm, send_head);
-    return cudaGetLastError();
+    const int64_t grid1 = p.chan_blocks + p.rank_blocks + p.expert_blocks;
+    e = launch_pdl(notify_count_kernel, static_cast<unsigned>(grid1), p.threads, smem_count, stream, s.P,
+                   s.E, s.num_channels, s.expert_alignment, T, p.rank_major, p.chan_blocks, p.rank_blocks,
+                   ntpr, ntpe, itr, rpm, nrt, nrtpe, ccount);
+    if (e != cudaSuccess) return e;
+    const int64_t grid2 = p.chan_blocks + p.tail_blocks;
+    return launch_pdl(notify_head_kernel, static_cast<unsigned>(grid2), p.threads, smem_head, stream, s.P, s.E,
+                      s.num_channels, T, p.rank_major, p.chan_blocks, itr, static_cast<const int32_t*>(rpm),
+                      static_cast<const int32_t*>(nrt), static_cast<const int32_t*>(nrtpe),
+                      static_cast<const int32_t*>(ccount), cpm, rcpm, send_head, reo, part_row_base);
 }
 
 }  // namespace moe

@@ -25,6 +25,7 @@ pad_kernel(int32_t P, int32_t K, int64_t payload_bytes, int64_t stride, int64_t 
            int64_t triple_off, bool quant, const int32_t* __restrict__ nrt,
            const int64_t* __restrict__ prb, uint8_t* __restrict__ arena, int64_t arena_rows,
            int32_t* __restrict__ src_idx, int32_t* __restrict__ tk_idx, float* __restrict__ tk_w) {
+    pdl_wait_then_release();
     const int d = blockIdx.x / kPadStripes, stripe = blockIdx.x % kPadStripes;
     const int64_t lo = prb[d] + (nrt[d] > 0 ? static_cast<int64_t>(nrt[d]) : 0);
     int64_t hi = prb[d + 1];
@@ -60,10 +61,9 @@ cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* pr
     const int64_t elt = s.quant ? 1 : 2;
     const int64_t scale_off = round_up(static_cast<int64_t>(s.H) * elt, 32);
     const int64_t stride = round_up(scale_off + 44, 512);
-    pad_kernel<<<static_cast<unsigned>(s.P) * kPadStripes, kPadThreads, 0, stream>>>(
-        s.P, s.K, static_cast<int64_t>(s.H) * elt, stride, scale_off, scale_off + 32, s.quant != 0, nrt,
-        prb, arena, arena_rows, src_idx, tk_idx, tk_w);
-    return cudaGetLastError();
+    return launch_pdl(pad_kernel, static_cast<unsigned>(s.P) * kPadStripes, kPadThreads, 0, stream, s.P, s.K,
+                      static_cast<int64_t>(s.H) * elt, stride, scale_off, scale_off + 32, s.quant != 0, nrt, prb,
+                      arena, arena_rows, src_idx, tk_idx, tk_w);
 }
 
 }  // namespace moe
