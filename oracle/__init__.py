@@ -63,6 +63,14 @@ def _load():
     lib.oracle_combine.restype = i32
     lib.oracle_combine.argtypes = [i32, i32, i64, i32, i32, vp, i64, vp, i64, vp, vp,
                                    vp, vp, vp, i64]
+    lib.oracle_notify_expert.restype = None
+    lib.oracle_notify_expert.argtypes = [i32, i32, i64, i32, vp, vp, vp, vp, vp]
+    lib.oracle_dispatch_expert.restype = i32
+    lib.oracle_dispatch_expert.argtypes = [i32, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64,
+                                           vp, vp, vp, i64]
+    lib.oracle_combine_expert.restype = i32
+    lib.oracle_combine_expert.argtypes = [i32, i32, i64, i32, i32, vp, i64, vp, i64, vp, vp, vp, vp,
+                                          vp, i64]
     lib.oracle_pad_partitions.restype = None
     lib.oracle_pad_partitions.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, vp, vp]
     lib.oracle_bf16_round.restype = None
@@ -183,6 +191,53 @@ def combine(P: int, E: int, H: int, y: np.ndarray, y_row_stride: int, part_row_b
     err = _load().oracle_combine(P, E, S, K, H, _p(y), int(y_row_stride), _p(prb), int(arena_rows),
                                  _p(send_head), _p(topk_idx), _p(w), _p(out),
                                  _p(tok), 0 if tok is None else int(tok.shape[0]))
+    return dict(out=out, err=int(err))
+
+
+def notify_expert(P: int, E: int, topk_idx: np.ndarray, num_recv_tokens_per_expert: np.ndarray,
+                  recv_expert_offset: np.ndarray) -> dict:
+    """Expert-major receive rows of every (token, k) slot and the partition bases."""
+    idx = _c(topk_idx, np.int32)
+    S, K = idx.shape
+    out = dict(slot_row=np.empty((S, K), np.int32), expert_part_base=np.empty((P + 1,), np.int64))
+    _load().oracle_notify_expert(P, E, S, K, _p(idx), _p(_c(num_recv_tokens_per_expert, np.int32)),
+                                 _p(_c(recv_expert_offset, np.int32)), _p(out["slot_row"]),
+                                 _p(out["expert_part_base"]))
+    return out
+
+
+def dispatch_expert(P: int, E: int, H: int, quant: int, x_bits, topk_idx, topk_weights, slot_row,
+                    expert_part_base, arena_rows: int, tokens=None, arena=None) -> dict:
+    x_bits = _c(x_bits, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    S, K = idx.shape
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    stride = slot_stride(H, quant)
+    if arena is None:
+        arena = np.zeros((arena_rows, stride), np.uint8)
+    out = dict(arena=arena, recv_src_idx=np.full((arena_rows,), -7, np.int32),
+               recv_weight=np.full((arena_rows,), -7.0, np.float32))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    err = _load().oracle_dispatch_expert(
+        P, E, S, K, H, quant, _p(x_bits), _p(idx), _p(w), _p(_c(slot_row, np.int32)),
+        _p(_c(expert_part_base, np.int64)), _p(arena), int(arena_rows), _p(out["recv_src_idx"]),
+        _p(out["recv_weight"]), _p(tok), 0 if tok is None else int(tok.shape[0]))
+    out["err"] = int(err)
+    return out
+
+
+def combine_expert(P: int, E: int, H: int, y, y_row_stride: int, expert_part_base, arena_rows: int,
+                   slot_row, topk_idx, topk_weights, tokens=None) -> dict:
+    y = np.ascontiguousarray(y).view(np.uint8)
+    idx = _c(topk_idx, np.int32)
+    S, K = idx.shape
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    out = np.zeros((S, H), np.uint16)
+    tok = None if tokens is None else _c(tokens, np.int64)
+    err = _load().oracle_combine_expert(P, E, S, K, H, _p(y), int(y_row_stride),
+                                        _p(_c(expert_part_base, np.int64)), int(arena_rows),
+                                        _p(_c(slot_row, np.int32)), _p(idx), _p(w), _p(out), _p(tok),
+                                        0 if tok is None else int(tok.shape[0]))
     return dict(out=out, err=int(err))
 
 

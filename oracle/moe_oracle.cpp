@@ -345,6 +345,124 @@ int32_t oracle_combine(int32_t P, int32_t E, int64_t S, int32_t K, int32_t H,
     return err;
 }
 
+// ---- Expert-major receive layout --------------------------------------------
+// "HCCL Window 模式 (Non-SHMEM) 代码深度剖析", section 3.6 (InputToShare): each
+// (token, k) slot is copied to hOutGMAlignSize * (dstExpertOffset +
+// curExpertCnt) of its expert's rank, the triple carrying that slot's k; and
+// section 7.8 (ReadBufferAndWeightedSum): the owner sums the K returned rows,
+// weight by weight, in k order. Inside rank d, expert l's rows start at
+// recv_expert_offset[d][l] (its aligned count's exclusive scan, "internode.cu"
+// section 1) and hold the expert's slots in (token, k) order.
+
+// slot_row[g][k] = recv_expert_offset[d][l] + (slots with the same expert that
+// come before (g, k) in (token, k) order), or -1 for a masked / invalid slot.
+// expert_part_base = exclusive scan over ranks of sum_l num_recv_tokens_per_expert[d][l].
+void oracle_notify_expert(int32_t P, int32_t E, int64_t S, int32_t K, const int32_t* topk_idx,
+                          const int32_t* num_recv_tokens_per_expert, const int32_t* recv_expert_offset,
+                          int32_t* slot_row, int64_t* expert_part_base) {
+    const int32_t epr = E / P;
+    std::vector<int32_t> counter(E, 0);
+    for (int64_t g = 0; g < S; ++g) {
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = topk_idx[g * K + k];
+            if (e < 0 || e >= E) {
+                slot_row[g * K + k] = -1;
+                continue;
+            }
+            slot_row[g * K + k] = recv_expert_offset[e] + counter[e];
+            counter[e] += 1;
+        }
+    }
+    expert_part_base[0] = 0;
+    for (int32_t d = 0; d < P; ++d) {
+        int64_t total = 0;
+        for (int32_t l = 0; l < epr; ++l) total += num_recv_tokens_per_expert[d * epr + l];
+        expert_part_base[d + 1] = expert_part_base[d] + total;
+    }
+}
+
+// One slot per valid (g, k): row expert_part_base[d] + slot_row[g][k] receives
+// the payload (as in oracle_dispatch), the triple (g / T, g % T, k),
+// recv_src_idx = g % T and recv_weight = topk_weights[g][k] (side arrays may
+// be NULL). Rows outside the partition or the arena are skipped: return 3.
+int32_t oracle_dispatch_expert(int32_t P, int32_t E, int64_t S, int32_t K, int32_t H, int32_t quant,
+                               const uint16_t* x, const int32_t* topk_idx, const float* topk_weights,
+                               const int32_t* slot_row, const int64_t* expert_part_base,
+                               uint8_t* arena, int64_t arena_rows, int32_t* recv_src_idx,
+                               float* recv_weight, const int64_t* tokens, int64_t n_tokens) {
+    const int32_t epr = E / P;
+    const int64_t T = S / P;
+    const int64_t stride = oracle_slot_stride(H, quant);
+    const int64_t elt = quant ? 1 : 2;
+    const int64_t scale_off = ceil_to(static_cast<int64_t>(H) * elt, 32);
+    const int64_t triple_off = scale_off + 32;
+    int32_t err = 0;
+    std::vector<int8_t> q(H);
+    const int64_t count = tokens ? n_tokens : S;
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t g = tokens ? tokens[i] : i;
+        float scale = 0.0f;
+        if (quant) scale = oracle_quantize_row(H, x + g * H, q.data());
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = topk_idx[g * K + k];
+            const int32_t sr = slot_row[g * K + k];
+            if (e < 0 || e >= E || sr < 0) continue;
+            const int32_t d = e / epr;
+            if (sr >= expert_part_base[d + 1] - expert_part_base[d]) { err = 3; continue; }
+            const int64_t row = expert_part_base[d] + sr;
+            if (row >= arena_rows) { err = 3; continue; }
+            uint8_t* slot = arena + row * stride;
+            if (quant) {
+                std::memcpy(slot, q.data(), H);
+                std::memcpy(slot + scale_off, &scale, 4);
+            } else {
+                std::memcpy(slot, x + g * H, static_cast<size_t>(H) * 2);
+            }
+            const int32_t triple[3] = {static_cast<int32_t>(g / T), static_cast<int32_t>(g % T), k};
+            std::memcpy(slot + triple_off, triple, 12);
+            if (recv_src_idx) recv_src_idx[row] = static_cast<int32_t>(g % T);
+            if (recv_weight) recv_weight[row] = topk_weights ? topk_weights[g * K + k] : 1.0f;
+        }
+    }
+    return err;
+}
+
+// out[g] = bf16_rne( sum over k ascending with a valid slot of
+//                    w[g][k] * f32(y[expert_part_base[d] + slot_row[g][k]]) ),
+// binary32 accumulator from +0, product and sum rounded separately; NULL
+// weights mean w = 1.
+int32_t oracle_combine_expert(int32_t P, int32_t E, int64_t S, int32_t K, int32_t H,
+                              const uint8_t* y, int64_t y_row_stride, const int64_t* expert_part_base,
+                              int64_t arena_rows, const int32_t* slot_row, const int32_t* topk_idx,
+                              const float* topk_weights, uint16_t* out, const int64_t* tokens,
+                              int64_t n_tokens) {
+    const int32_t epr = E / P;
+    int32_t err = 0;
+    std::vector<float> acc(H);
+    const int64_t count = tokens ? n_tokens : S;
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t g = tokens ? tokens[i] : i;
+        std::fill(acc.begin(), acc.end(), 0.0f);
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t e = topk_idx[g * K + k];
+            const int32_t sr = slot_row[g * K + k];
+            if (e < 0 || e >= E || sr < 0) continue;
+            const int32_t d = e / epr;
+            if (sr >= expert_part_base[d + 1] - expert_part_base[d]) { err = 3; continue; }
+            const int64_t row = expert_part_base[d] + sr;
+            if (row >= arena_rows) { err = 3; continue; }
+            const float w = topk_weights ? topk_weights[g * K + k] : 1.0f;
+            const uint16_t* yrow = reinterpret_cast<const uint16_t*>(y + row * y_row_stride);
+            for (int32_t h = 0; h < H; ++h) {
+                float prod = w * bf16_bits_to_float(yrow[h]);
+                acc[h] = acc[h] + prod;
+            }
+        }
+        for (int32_t h = 0; h < H; ++h) out[g * H + h] = float_to_bf16_bits_rne(acc[h]);
+    }
+    return err;
+}
+
 // Fixed-length receive partitions ("Ascend DeepEP MoE Dispatch Optimization",
 // section "输出长度有动态和固定两种模式": with a fixed output length the rows
 // past the received count are padding -- x, scales and weights 0, topk_idx
