@@ -57,6 +57,20 @@ def combine_bytes(S, P, K, H, R):
     return R * 2 * H + S * 2 * H + S * P * 4 + S * K * 8
 
 
+def dispatch_expert_bytes(S, K, H, R, quant):
+    """Expert-major layout: read x once, write one slot per (token, k) with its
+    triple, recv_src_idx and recv_weight; read topk ids, weights, slot rows."""
+    payload = H if quant else 2 * H
+    meta = 16 if quant else 12
+    return 2 * S * H + R * (payload + meta) + R * 8 + S * K * 12
+
+
+def combine_expert_bytes(S, K, H, R):
+    """Expert-major layout: read every slot row once, write out, read topk ids,
+    weights and slot rows."""
+    return R * 2 * H + S * 2 * H + S * K * 12
+
+
 # --------------------------------------------------------------------------
 # Multi-rank helpers (also exercised on CPU with gloo).
 
@@ -175,7 +189,7 @@ def recorded_traffic(workload: str, kernel: str):
 # CPU oracle on a bounded sample (reference arm and cpu_baseline).
 
 def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int = 1000,
-                  workload=None):
+                  workload=None, layout: str = "rank"):
     """Time the oracle's full path on a bounded sample of the workload: the same
     shape with T_sample tokens per rank. Returns tokens/s, passes, seconds and
     a description of the sample."""
@@ -189,14 +203,23 @@ def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int 
         lay = oracle.layout(w.P, w.E, w.topk_idx)
         nt = oracle.notify(w.P, w.E, w.C, w.expert_alignment, lay["num_tokens_per_rank"],
                            lay["num_tokens_per_expert"], lay["is_token_in_rank"])
-        rows = int(nt["part_row_base"][-1])
-        dis = oracle.dispatch(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
-                              nt["send_head"], nt["part_row_base"], rows)
-        oracle.combine(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0), nt["part_row_base"],
-                       rows, nt["send_head"], w.topk_idx, w.topk_weights)
+        if layout == "expert":
+            ex = oracle.notify_expert(w.P, w.E, w.topk_idx, nt["num_recv_tokens_per_expert"],
+                                      nt["recv_expert_offset"])
+            rows = int(ex["expert_part_base"][-1])
+            dis = oracle.dispatch_expert(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
+                                         ex["slot_row"], ex["expert_part_base"], rows)
+            oracle.combine_expert(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0),
+                                  ex["expert_part_base"], rows, ex["slot_row"], w.topk_idx, w.topk_weights)
+        else:
+            rows = int(nt["part_row_base"][-1])
+            dis = oracle.dispatch(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
+                                  nt["send_head"], nt["part_row_base"], rows)
+            oracle.combine(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0), nt["part_row_base"],
+                           rows, nt["send_head"], w.topk_idx, w.topk_weights)
         t_total += time.perf_counter() - t0
         passes += 1
-    sample = (f"{name} with T={w.T} tokens per rank (S={w.S}, {passes} pass(es)); "
+    sample = (f"{name} ({layout} layout) with T={w.T} tokens per rank (S={w.S}, {passes} pass(es)); "
               "single-threaded oracle: layout+notify+dispatch+combine")
     return w.S * passes / t_total, passes, t_total, sample
 
@@ -208,10 +231,11 @@ def run_reference(args, world, rank):
 
     w = inputs.workload(args.workload, T=args.ref_tokens)
     for _ in range(args.warmup):
-        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w)
+        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w, layout=args.layout)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, _, _, sample = oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w)
+        _, _, _, sample = oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w,
+                                        layout=args.layout)
     elapsed = time.perf_counter() - t0
     value = w.S * args.steps / elapsed
     sample = sample.replace("1 pass(es)", f"{args.steps} timed steps of 1 pass")
@@ -220,7 +244,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(args.workload),
+        "config": dict(workload_config(args.workload), layout=args.layout),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -253,7 +277,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     w = inputs.workload(args.workload, T=args.tokens_per_rank)
     shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, w.quant)
-    buf = moe.Buffers(shape, dev, side_arrays=True)
+    buf = moe.Buffers(shape, dev, side_arrays=args.layout == "rank",
+                      arena_rows=1 if args.layout == "expert" else None)
     x_host = torch.from_numpy(w.x_bits.view(np.int16)).pin_memory()
     idx_host = torch.from_numpy(w.topk_idx).pin_memory()
     wts_host = torch.from_numpy(w.topk_weights).pin_memory()
@@ -264,25 +289,49 @@ def run_ours(args, world, rank, local):
     out_host = torch.empty((w.S, w.H), dtype=torch.int16).pin_memory()
     stream = torch.cuda.current_stream(dev)
 
+    expert = args.layout == "expert"
+    if expert:
+        buf._expert_buffers()
+    # int8 slots: combine reads bf16 expert outputs. The expert stage is not
+    # part of the path, so one bf16 output arena (random rows, seeded) is
+    # made once here and every step's combine reads it.
+    y_out, y_stride = None, None
+    if w.quant:
+        rows_alloc = buf.expert_rows if expert else buf.arena_rows
+        gen = torch.Generator(device=dev).manual_seed(0)
+        y_out = torch.empty((max(rows_alloc, 1), w.H), dtype=torch.bfloat16, device=dev)
+        y_out.normal_(generator=gen)
+        y_out = y_out.view(torch.int16)
+        y_stride = 2 * w.H
+
     def step(ev=None):
-        if ev is None:
-            buf.step(x, idx, wts, out, stream)
-            return
-        ev[0].record(stream)
+        if ev is not None:
+            ev[0].record(stream)
         buf.layout(idx, stream)
         buf.notify(stream)
-        ev[1].record(stream)
-        buf.dispatch(x, idx, wts, stream)
-        ev[2].record(stream)
-        buf.combine(out, idx, wts, stream=stream)
-        ev[3].record(stream)
+        if expert:
+            buf.notify_expert(idx, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if expert:
+            buf.dispatch_expert(x, idx, wts, stream)
+        else:
+            buf.dispatch(x, idx, wts, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        if expert:
+            buf.combine_expert(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=stream)
+        else:
+            buf.combine(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if int(buf.err[0].item()) != 0:
         raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")
-    R = int(buf.part_row_base[-1].item())
+    R = int((buf.expert_part_base if expert else buf.part_row_base)[-1].item())
 
     # --- device-timed region: whole steps --------------------------------
     uuid = None
@@ -317,8 +366,12 @@ def run_ours(args, world, rank, local):
     t_disp = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     t_comb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
     peak, peak_kind = measured_peaks()
-    db = dispatch_bytes(w.S, w.P, w.K, w.H, R, w.quant)
-    cb = combine_bytes(w.S, w.P, w.K, w.H, R)
+    if expert:
+        db = dispatch_expert_bytes(w.S, w.K, w.H, R, w.quant)
+        cb = combine_expert_bytes(w.S, w.K, w.H, R)
+    else:
+        db = dispatch_bytes(w.S, w.P, w.K, w.H, R, w.quant)
+        cb = combine_bytes(w.S, w.P, w.K, w.H, R)
     disp_gbs = db / t_disp / 1e9
     comb_gbs = cb / t_comb / 1e9
     dominant = "dispatch" if t_disp >= t_comb else "combine"
@@ -349,7 +402,8 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, passes, secs, sample = oracle_sample(args.workload, args.ref_tokens, args.cpu_seconds)
+        tps, passes, secs, sample = oracle_sample(args.workload, args.ref_tokens, args.cpu_seconds,
+                                                  layout=args.layout)
         cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
 
     if rank != 0:
@@ -358,8 +412,8 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(args.workload, args.tokens_per_rank),
-        "gpu_launches": 6 * args.steps,
+        "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout),
+        "gpu_launches": (9 if expert else 6) * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "traffic": recorded_traffic(args.workload, kname),
@@ -391,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
+                    help="receive layout: one row per (token, rank), or one per (token, k) grouped by expert")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="override T (a smaller case of the same workload, e.g. for profiling)")
     ap.add_argument("--ref-tokens", type=int, default=512,

@@ -80,8 +80,15 @@ int64_t moe_scratch_bytes(const moe_shape* s) {
     if (moe_check_shape(s) != MOE_OK) return -1;
     const int64_t a = layout_plan(*s).scratch_bytes;
     const int64_t b = notify_scratch_bytes(*s);
-    const int64_t m = a > b ? a : b;
+    const int64_t c = notify_expert_scratch_bytes(*s);
+    int64_t m = a > b ? a : b;
+    m = m > c ? m : c;
     return m > 256 ? m : 256;
+}
+
+int64_t moe_max_expert_rows(const moe_shape* s) {
+    if (moe_check_shape(s) != MOE_OK) return -1;
+    return static_cast<int64_t>(s->S) * s->K + static_cast<int64_t>(s->E) * (s->expert_alignment - 1);
 }
 
 int64_t moe_max_recv_rows(const moe_shape* s) {
@@ -207,6 +214,96 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
     a.out = out;
     a.err = err;
     return from_cuda(launch_combine(s, a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_notify_expert(const moe_shape* shape, const int32_t* topk_idx,
+                             const int32_t* num_recv_tokens_per_expert, const int32_t* recv_expert_offset,
+                             int32_t* slot_row, int64_t* expert_part_base, void* scratch,
+                             int64_t scratch_bytes, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (!ok_ptr(topk_idx, S * s.K, 16) || !ok_ptr(num_recv_tokens_per_expert, 1, 16) ||
+        !ok_ptr(recv_expert_offset, 1, 16) || !ok_ptr(slot_row, S * s.K, 16) ||
+        !ok_ptr(expert_part_base, 1, 16) || !ok_ptr(scratch, 1, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_scratch_bytes(shape)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_notify_expert(s, topk_idx, num_recv_tokens_per_expert, recv_expert_offset,
+                                          slot_row, expert_part_base, scratch,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_expert(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                               const float* topk_weights, const int32_t* slot_row,
+                               const int64_t* expert_part_base, void* recv_arena, int64_t arena_rows,
+                               int32_t* recv_src_idx, float* recv_weight, int32_t* err, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (arena_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(x, S * s.H, 16) || !ok_ptr(topk_idx, S * s.K, 16) || !ok_ptr(slot_row, S * s.K, 16) ||
+        !ok_ptr(expert_part_base, 1, 16) || !ok_ptr(recv_arena, arena_rows, 16) ||
+        !ok_opt(recv_src_idx, 16) || !ok_opt(recv_weight, 16) || !ok_opt(topk_weights, 16) ||
+        !ok_opt(err, 4))
+        return MOE_ERR_INVALID_ARG;
+    DispatchArgs a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.K = s.K;
+    a.H = s.H;
+    a.epr = s.E / s.P;
+    a.S = S;
+    a.T = S / s.P;
+    a.x = x;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.part_row_base = expert_part_base;
+    a.arena = static_cast<uint8_t*>(recv_arena);
+    a.arena_rows = arena_rows;
+    a.stride = moe_slot_stride(s.H, s.quant);
+    a.scale_off = round_up(static_cast<int64_t>(s.H) * (s.quant ? 1 : 2), 32);
+    a.triple_off = a.scale_off + 32;
+    a.recv_src_idx = recv_src_idx;
+    a.err = err;
+    a.row_bytes = static_cast<uint32_t>(s.H) * 2u;
+    a.slot_row = slot_row;
+    a.recv_weight = recv_weight;
+    return from_cuda(launch_dispatch_expert(s, a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_expert(const moe_shape* shape, const void* y, int64_t y_row_stride,
+                              const int64_t* expert_part_base, int64_t arena_rows, const int32_t* slot_row,
+                              const int32_t* topk_idx, const float* topk_weights, uint16_t* out,
+                              int32_t* err, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int64_t S = s.S;
+    if (arena_rows < 0 || y_row_stride < 2 * static_cast<int64_t>(s.H) || y_row_stride % 16 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(y, arena_rows, 16) || !ok_ptr(expert_part_base, 1, 16) || !ok_ptr(slot_row, S * s.K, 16) ||
+        !ok_ptr(topk_idx, S * s.K, 16) || !ok_opt(topk_weights, 16) || !ok_ptr(out, S * s.H, 16) ||
+        !ok_opt(err, 4))
+        return MOE_ERR_INVALID_ARG;
+    CombineArgs a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.K = s.K;
+    a.H = s.H;
+    a.epr = s.E / s.P;
+    a.S = S;
+    a.y = static_cast<const uint8_t*>(y);
+    a.y_stride = y_row_stride;
+    a.part_row_base = expert_part_base;
+    a.arena_rows = arena_rows;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.out = out;
+    a.err = err;
+    a.slot_row = slot_row;
+    return from_cuda(launch_combine_expert(s, a, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_tokens,

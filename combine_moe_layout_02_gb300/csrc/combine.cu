@@ -53,15 +53,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // One lane's routing words of a token: send_head of rank `lane` (the first 32
 // ranks; further ranks are read during the compaction) and Top-K slot `lane`.
 struct TokenRoute {
-    int32_t sh0;
+    int32_t sh0;  // rank layout: send_head of rank `lane`; expert layout: slot_row of slot `lane`
     int32_t idx;
     float w;
 };
 
+template <bool EXPERT>
 __device__ __forceinline__ TokenRoute load_route(const CombineArgs& a, int64_t g, int lane) {
     TokenRoute r{-1, -1, 0.f};
     if (g < a.S) {
-        if (lane < a.P) r.sh0 = __ldg(a.send_head + g * a.P + lane);
+        if (EXPERT) {
+            if (lane < a.K) r.sh0 = __ldg(a.slot_row + g * a.K + lane);
+        } else {
+            if (lane < a.P) r.sh0 = __ldg(a.send_head + g * a.P + lane);
+        }
         if (lane < a.K) {
             r.idx = __ldg(a.topk_idx + g * a.K + lane);
             if (a.topk_weights) r.w = __ldg(a.topk_weights + g * a.K + lane);
@@ -70,7 +75,7 @@ __device__ __forceinline__ TokenRoute load_route(const CombineArgs& a, int64_t g
     return r;
 }
 
-template <int MAXR>
+template <int MAXR, bool EXPERT>
 __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_kernel(const CombineArgs a) {
     pdl_wait_then_release();
     extern __shared__ __align__(16) int64_t prb[];  // [P+1]
@@ -80,32 +85,46 @@ __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_k
     const int nchunks = a.H / 8;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5);
-    TokenRoute cur = load_route(a, g, lane);
+    TokenRoute cur = load_route<EXPERT>(a, g, lane);
     for (; g < a.S; g += warps_total) {
-        const TokenRoute nxt = load_route(a, g + warps_total, lane);
+        const TokenRoute nxt = load_route<EXPERT>(a, g + warps_total, lane);
         const int32_t dk = (cur.idx >= 0 && cur.idx < a.E) ? cur.idx / a.epr : -1;
         // Compaction: lane r ends up holding the r-th valid rank's row and weight.
         uint64_t my_row = 0;
         float my_coef = 0.f;
         int n = 0;
-        for (int d0 = 0; d0 < a.P; d0 += 32) {
+        // Candidates: ranks d = d0 + lane (rank layout) or slots k = lane
+        // (expert layout, K <= 32: one pass).
+        const int ncand = EXPERT ? a.K : a.P;
+        for (int d0 = 0; d0 < ncand; d0 += 32) {
             const int d = d0 + lane;
-            const int32_t sh = d0 == 0 ? cur.sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
             bool valid = false;
             int64_t row = 0;
-            if (sh >= 0) {
-                const int64_t lo = prb[d], hi = prb[d + 1];
-                row = lo + sh;
-                valid = sh < hi - lo && row >= 0 && row < a.arena_rows;
-                if (!valid) raise_error(a.err, MOE_ERR_CAPACITY);
-            }
             float c = 0.f;
-            for (int k = 0; k < a.K; ++k) {
-                const int32_t dkk = __shfl_sync(0xffffffffu, dk, k);
-                const float wk = __shfl_sync(0xffffffffu, cur.w, k);
-                if (dkk == d) c = __fadd_rn(c, wk);
+            if (EXPERT) {
+                const int32_t sr = cur.sh0;
+                if (dk >= 0 && sr >= 0) {
+                    const int64_t lo = prb[dk], hi = prb[dk + 1];
+                    row = lo + sr;
+                    valid = sr < hi - lo && row >= 0 && row < a.arena_rows;
+                    if (!valid) raise_error(a.err, MOE_ERR_CAPACITY);
+                }
+                c = a.topk_weights ? cur.w : 1.f;
+            } else {
+                const int32_t sh = d0 == 0 ? cur.sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
+                if (sh >= 0) {
+                    const int64_t lo = prb[d], hi = prb[d + 1];
+                    row = lo + sh;
+                    valid = sh < hi - lo && row >= 0 && row < a.arena_rows;
+                    if (!valid) raise_error(a.err, MOE_ERR_CAPACITY);
+                }
+                for (int k = 0; k < a.K; ++k) {
+                    const int32_t dkk = __shfl_sync(0xffffffffu, dk, k);
+                    const float wk = __shfl_sync(0xffffffffu, cur.w, k);
+                    if (dkk == d) c = __fadd_rn(c, wk);
+                }
+                if (!a.topk_weights) c = 1.f;
             }
-            if (!a.topk_weights) c = 1.f;
             const uint64_t rp = reinterpret_cast<uint64_t>(a.y + row * a.y_stride);
             const uint32_t bal = __ballot_sync(0xffffffffu, valid);
             const int cnt = __popc(bal);
@@ -173,11 +192,11 @@ __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_k
     }
 }
 
-template <int MAXR>
+template <int MAXR, bool EXPERT>
 cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(a.P + 1) * 8;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<MAXR>,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<MAXR, EXPERT>,
                                                                   kCombineThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
@@ -185,19 +204,27 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int64_t needed = ceil_div(a.S, warps_per_block);
     if (grid > needed) grid = needed;
-    return launch_pdl(combine_kernel<MAXR>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a);
+    return launch_pdl(combine_kernel<MAXR, EXPERT>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a);
+}
+
+template <bool EXPERT>
+cudaError_t launch_combine_mode(const CombineArgs& a, int maxr, cudaStream_t stream) {
+    if (a.S == 0) return cudaSuccess;
+    if (maxr <= 1) return launch_combine_t<1, EXPERT>(a, stream);
+    if (maxr <= 2) return launch_combine_t<2, EXPERT>(a, stream);
+    if (maxr <= 4) return launch_combine_t<4, EXPERT>(a, stream);
+    if (maxr <= 8) return launch_combine_t<8, EXPERT>(a, stream);
+    return launch_combine_t<16, EXPERT>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, CombineArgs a, cudaStream_t stream) {
-    if (a.S == 0) return cudaSuccess;
-    const int maxr = s.K < s.P ? s.K : s.P;  // distinct ranks of one token
-    if (maxr <= 1) return launch_combine_t<1>(a, stream);
-    if (maxr <= 2) return launch_combine_t<2>(a, stream);
-    if (maxr <= 4) return launch_combine_t<4>(a, stream);
-    if (maxr <= 8) return launch_combine_t<8>(a, stream);
-    return launch_combine_t<16>(a, stream);
+    return launch_combine_mode<false>(a, s.K < s.P ? s.K : s.P, stream);  // distinct ranks of a token
+}
+
+cudaError_t launch_combine_expert(const moe_shape& s, CombineArgs a, cudaStream_t stream) {
+    return launch_combine_mode<true>(a, s.K, stream);  // one row per slot
 }
 
 }  // namespace moe

@@ -120,6 +120,38 @@ __device__ __forceinline__ uint8_t* slot_of(const DispatchArgs& a, const int64_t
     return nullptr;
 }
 
+// Expert-major layout: destination row of slot (g, lane), or nullptr. Lanes
+// k < K carry slot k; the row is part_row_base[d] + slot_row[g][k].
+__device__ __forceinline__ uint8_t* expert_slot_of(const DispatchArgs& a, const int64_t* prb, int64_t g,
+                                                   int lane, int64_t* row_out) {
+    if (lane >= a.K) return nullptr;
+    const int32_t e = __ldg(a.topk_idx + g * a.K + lane);
+    const int32_t sr = __ldg(a.slot_row + g * a.K + lane);
+    if (e < 0 || e >= a.E || sr < 0) return nullptr;
+    const int d = e / a.epr;
+    uint8_t* dst = slot_of(a, prb, d, sr);
+    if (dst) *row_out = prb[d] + sr;
+    return dst;
+}
+
+// Expert-major layout: triple (source rank, source-local token, k) and side
+// arrays of each slot of token g; lane k writes slot k's.
+__device__ void write_slot_meta(const DispatchArgs& a, const int64_t* prb, int64_t g, int lane) {
+    if (lane >= a.K) return;
+    const int32_t e = __ldg(a.topk_idx + g * a.K + lane);
+    const int32_t sr = __ldg(a.slot_row + g * a.K + lane);
+    if (e < 0 || e >= a.E || sr < 0) return;
+    const int d = e / a.epr;
+    const int64_t lo = prb[d], hi = prb[d + 1], row = lo + sr;
+    if (sr >= hi - lo || row < 0 || row >= a.arena_rows) return;  // reported by the copy path
+    const int32_t t = static_cast<int32_t>(g % a.T);
+    int4* trip = reinterpret_cast<int4*>(a.arena + row * a.stride + a.triple_off);
+    trip[0] = make_int4(static_cast<int32_t>(g / a.T), t, lane, 0);
+    trip[1] = make_int4(0, 0, 0, 0);
+    if (a.recv_src_idx) a.recv_src_idx[row] = t;
+    if (a.recv_weight) a.recv_weight[row] = a.topk_weights ? __ldg(a.topk_weights + g * a.K + lane) : 1.f;
+}
+
 __device__ void load_prb_and_init(const DispatchArgs& a, int64_t* prb, uint64_t* bars) {
     for (int i = threadIdx.x; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
     if (threadIdx.x == 0) {
@@ -135,6 +167,7 @@ __device__ void drain_loads(uint64_t* bars, int stages, int64_t first, int64_t l
     for (int64_t j = first; j <= last_issued; ++j) mbar_wait(&bars[j % stages], (j / stages) & 1);
 }
 
+template <bool EXPERT>
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchArgs a) {
     pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
@@ -150,8 +183,12 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
     const int64_t n_local = blockIdx.x < a.S ? (a.S - 1 - blockIdx.x) / G + 1 : 0;
 
     if (warp != 0) {
-        for (int64_t i = warp - 1; i < n_local; i += nwarps - 1)
-            write_token_meta(a, prb, blockIdx.x + i * G, lane);
+        for (int64_t i = warp - 1; i < n_local; i += nwarps - 1) {
+            if constexpr (EXPERT)
+                write_slot_meta(a, prb, blockIdx.x + i * G, lane);
+            else
+                write_token_meta(a, prb, blockIdx.x + i * G, lane);
+        }
         return;
     }
 
@@ -172,19 +209,30 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
     for (; i < n_local; ++i) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
-        const int32_t sh0 = lane < a.P ? __ldg(a.send_head + g * a.P + lane) : -1;
+        int32_t sh0 = -1;
+        uint8_t* xdst = nullptr;
+        if constexpr (EXPERT) {
+            int64_t row;
+            xdst = expert_slot_of(a, prb, g, lane, &row);
+        } else {
+            sh0 = lane < a.P ? __ldg(a.send_head + g * a.P + lane) : -1;
+        }
         const bool ok = mbar_wait(&bars[slot], static_cast<uint32_t>((i / NS) & 1));
         if (__any_sync(0xffffffffu, !ok)) {
             failed = true;
             break;
         }
         const unsigned char* src = ring + static_cast<size_t>(slot) * RB;
-        for (int d0 = 0; d0 < a.P; d0 += 32) {
-            const int d = d0 + lane;
-            const int32_t sh = d0 == 0 ? sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
-            if (sh >= 0) {
-                uint8_t* dst = slot_of(a, prb, d, sh);
-                if (dst) bulk_store(dst, src, RB);
+        if constexpr (EXPERT) {
+            if (xdst) bulk_store(xdst, src, RB);
+        } else {
+            for (int d0 = 0; d0 < a.P; d0 += 32) {
+                const int d = d0 + lane;
+                const int32_t sh = d0 == 0 ? sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
+                if (sh >= 0) {
+                    uint8_t* dst = slot_of(a, prb, d, sh);
+                    if (dst) bulk_store(dst, src, RB);
+                }
             }
         }
         bulk_commit();
@@ -225,6 +273,7 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float scale, bool zer
     return (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8);
 }
 
+template <bool EXPERT>
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
     pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
@@ -300,21 +349,31 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                 last_issued = nxt;
             }
         }
-        for (int d = tid; d < a.P; d += nthreads) {
-            const int32_t sh = __ldg(a.send_head + g * a.P + d);
-            if (sh >= 0) {
-                uint8_t* dst = slot_of(a, prb, d, sh);
-                if (dst) {
-                    bulk_store(dst, q, static_cast<uint32_t>(a.H));
-                    // Scale plus zero padding: one whole 32-byte sector.
-                    int4* sc = reinterpret_cast<int4*>(dst + a.scale_off);
-                    sc[0] = make_int4(__float_as_int(scale), 0, 0, 0);
-                    sc[1] = make_int4(0, 0, 0, 0);
-                }
+        const int nfan = EXPERT ? a.K : a.P;
+        for (int d = tid; d < nfan; d += nthreads) {
+            uint8_t* dst = nullptr;
+            if constexpr (EXPERT) {
+                int64_t row;
+                dst = expert_slot_of(a, prb, g, d, &row);
+            } else {
+                const int32_t sh = __ldg(a.send_head + g * a.P + d);
+                if (sh >= 0) dst = slot_of(a, prb, d, sh);
+            }
+            if (dst) {
+                bulk_store(dst, q, static_cast<uint32_t>(a.H));
+                // Scale plus zero padding: one whole 32-byte sector.
+                int4* sc = reinterpret_cast<int4*>(dst + a.scale_off);
+                sc[0] = make_int4(__float_as_int(scale), 0, 0, 0);
+                sc[1] = make_int4(0, 0, 0, 0);
             }
         }
         bulk_commit();
-        if (warp == static_cast<int>(i % nwarps)) write_token_meta(a, prb, g, lane);
+        if (warp == static_cast<int>(i % nwarps)) {
+            if constexpr (EXPERT)
+                write_slot_meta(a, prb, g, lane);
+            else
+                write_token_meta(a, prb, g, lane);
+        }
         // The int8 buffer written two tokens from now is this token's partner:
         // its stores must have left shared memory before then.
         bulk_wait_read<1>();
@@ -328,7 +387,8 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
 
 }  // namespace
 
-cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
+template <bool EXPERT>
+cudaError_t launch_dispatch_mode(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
     if (a.S == 0) return cudaSuccess;
     const bool quant = s.quant != 0;
     // Ring depth: as many rows as fit in the ring budget, at least one more
@@ -338,8 +398,8 @@ cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t str
     stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
     a.stages = stages;
     const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
-    const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel)
-                           : reinterpret_cast<const void*>(dispatch_bf16_kernel);
+    const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel<EXPERT>)
+                           : reinterpret_cast<const void*>(dispatch_bf16_kernel<EXPERT>);
     const int threads = quant ? kInt8Threads : kBf16Threads;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L.total));
@@ -350,8 +410,17 @@ cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t str
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
     if (grid > a.S) grid = a.S;
-    if (quant) return launch_pdl(dispatch_int8_kernel, static_cast<unsigned>(grid), threads, L.total, stream, a);
-    return launch_pdl(dispatch_bf16_kernel, static_cast<unsigned>(grid), threads, L.total, stream, a);
+    if (quant)
+        return launch_pdl(dispatch_int8_kernel<EXPERT>, static_cast<unsigned>(grid), threads, L.total, stream, a);
+    return launch_pdl(dispatch_bf16_kernel<EXPERT>, static_cast<unsigned>(grid), threads, L.total, stream, a);
+}
+
+cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
+    return launch_dispatch_mode<false>(s, a, stream);
+}
+
+cudaError_t launch_dispatch_expert(const moe_shape& s, DispatchArgs a, cudaStream_t stream) {
+    return launch_dispatch_mode<true>(s, a, stream);
 }
 
 }  // namespace moe

@@ -183,8 +183,12 @@ struct DispatchArgs {
     int32_t* err;
     int32_t stages;
     uint32_t row_bytes;  // bf16 bytes of one source row, H * 2
+    // Expert-major layout only: one slot per (token, k).
+    const int32_t* slot_row;  // [S, K] row inside the destination rank's partition, or -1
+    float* recv_weight;       // [rows] the slot's Top-K weight (may be NULL)
 };
 cudaError_t launch_dispatch(const moe_shape& s, DispatchArgs a, cudaStream_t stream);
+cudaError_t launch_dispatch_expert(const moe_shape& s, DispatchArgs a, cudaStream_t stream);
 
 struct CombineArgs {
     int32_t P, E, K, H, epr;
@@ -198,8 +202,15 @@ struct CombineArgs {
     const float* topk_weights;
     uint16_t* out;
     int32_t* err;
+    const int32_t* slot_row;  // expert-major layout only
 };
 cudaError_t launch_combine(const moe_shape& s, CombineArgs a, cudaStream_t stream);
+cudaError_t launch_combine_expert(const moe_shape& s, CombineArgs a, cudaStream_t stream);
+
+int64_t notify_expert_scratch_bytes(const moe_shape& s);
+cudaError_t launch_notify_expert(const moe_shape& s, const int32_t* topk_idx, const int32_t* nrtpe,
+                                 const int32_t* reo, int32_t* slot_row, int64_t* expert_part_base,
+                                 void* scratch, cudaStream_t stream);
 
 cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* prb, uint8_t* arena,
                        int64_t arena_rows, int32_t* src_idx, int32_t* tk_idx, float* tk_w,

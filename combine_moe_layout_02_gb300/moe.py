@@ -25,7 +25,8 @@ MOE_ERR_INCONSISTENT = 7
 
 EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
-           "moe_layout_static_scratch", "moe_pad_partitions")
+           "moe_layout_static_scratch", "moe_pad_partitions", "moe_max_expert_rows",
+           "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert")
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
 MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -85,6 +86,14 @@ def lib() -> ctypes.CDLL:
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_combine.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+    L.moe_max_expert_rows.restype = i64
+    L.moe_max_expert_rows.argtypes = [sp]
+    L.moe_notify_expert.restype = i32
+    L.moe_notify_expert.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp]
+    L.moe_dispatch_expert.restype = i32
+    L.moe_dispatch_expert.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]
+    L.moe_combine_expert.restype = i32
+    L.moe_combine_expert.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
     L.moe_pad_partitions.restype = i32
     L.moe_pad_partitions.argtypes = [sp, vp, vp, vp, i64, vp, vp, vp, vp]
     L.moe_layout_static_scratch.restype = i32
@@ -181,6 +190,37 @@ def moe_combine(shape, y, y_row_stride, part_row_base, arena_rows, send_head, to
     _check(st, "moe_combine")
 
 
+def moe_max_expert_rows(shape: moe_shape) -> int:
+    return int(lib().moe_max_expert_rows(ctypes.byref(shape)))
+
+
+def moe_notify_expert(shape, topk_idx, num_recv_tokens_per_expert, recv_expert_offset, slot_row,
+                      expert_part_base, scratch, stream=None):
+    st = lib().moe_notify_expert(ctypes.byref(shape), _ptr(topk_idx), _ptr(num_recv_tokens_per_expert),
+                                 _ptr(recv_expert_offset), _ptr(slot_row), _ptr(expert_part_base),
+                                 _ptr(scratch), int(scratch.numel() * scratch.element_size()),
+                                 _stream(stream))
+    _check(st, "moe_notify_expert")
+
+
+def moe_dispatch_expert(shape, x, topk_idx, topk_weights, slot_row, expert_part_base, recv_arena,
+                        arena_rows, recv_src_idx, recv_weight, err, stream=None):
+    st = lib().moe_dispatch_expert(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(topk_weights),
+                                   _ptr(slot_row), _ptr(expert_part_base), _ptr(recv_arena),
+                                   int(arena_rows), _ptr(recv_src_idx), _ptr(recv_weight), _ptr(err),
+                                   _stream(stream))
+    _check(st, "moe_dispatch_expert")
+
+
+def moe_combine_expert(shape, y, y_row_stride, expert_part_base, arena_rows, slot_row, topk_idx,
+                       topk_weights, out, err, stream=None):
+    st = lib().moe_combine_expert(ctypes.byref(shape), _ptr(y), int(y_row_stride),
+                                  _ptr(expert_part_base), int(arena_rows), _ptr(slot_row),
+                                  _ptr(topk_idx), _ptr(topk_weights), _ptr(out), _ptr(err),
+                                  _stream(stream))
+    _check(st, "moe_combine_expert")
+
+
 def moe_pad_partitions(shape, num_recv_tokens, part_row_base, recv_arena, arena_rows,
                        recv_src_idx, recv_topk_idx, recv_topk_weights, stream=None):
     st = lib().moe_pad_partitions(ctypes.byref(shape), _ptr(num_recv_tokens), _ptr(part_row_base),
@@ -270,6 +310,38 @@ class Buffers:
         moe_pad_partitions(self.shape, self.num_recv_tokens, self.part_row_base, self.recv_arena,
                            self.arena_rows, self.recv_src_idx, self.recv_topk_idx,
                            self.recv_topk_weights, stream)
+
+    # ---- expert-major layout (after layout and notify) --------------------
+    def _expert_buffers(self, arena_rows=None):
+        import torch
+
+        if getattr(self, "slot_row", None) is not None:
+            return
+        s, dev = self.shape, self.device
+        self.slot_row = torch.empty((s.S, s.K), dtype=torch.int32, device=dev)
+        self.expert_part_base = torch.empty((s.P + 1,), dtype=torch.int64, device=dev)
+        self.expert_rows = moe_max_expert_rows(s) if arena_rows is None else int(arena_rows)
+        rows = max(self.expert_rows, 1)
+        self.expert_arena = torch.empty((rows, self.stride), dtype=torch.uint8, device=dev)
+        self.expert_src_idx = torch.empty((rows,), dtype=torch.int32, device=dev)
+        self.expert_weight = torch.empty((rows,), dtype=torch.float32, device=dev)
+
+    def notify_expert(self, topk_idx, stream=None, arena_rows=None):
+        self._expert_buffers(arena_rows)
+        moe_notify_expert(self.shape, topk_idx, self.num_recv_tokens_per_expert, self.recv_expert_offset,
+                          self.slot_row, self.expert_part_base, self.scratch, stream)
+
+    def dispatch_expert(self, x, topk_idx, topk_weights, stream=None):
+        moe_dispatch_expert(self.shape, x, topk_idx, topk_weights, self.slot_row, self.expert_part_base,
+                            self.expert_arena, self.expert_rows, self.expert_src_idx, self.expert_weight,
+                            self.err, stream)
+
+    def combine_expert(self, out, topk_idx, topk_weights, y=None, y_row_stride=None, stream=None):
+        """Per-slot combine; by default y is the expert-major arena (identity experts)."""
+        if y is None:
+            y, y_row_stride = self.expert_arena, self.stride
+        moe_combine_expert(self.shape, y, y_row_stride, self.expert_part_base, self.expert_rows,
+                           self.slot_row, topk_idx, topk_weights, out, self.err, stream)
 
     def step(self, x, topk_idx, topk_weights, out, stream=None):
         """One pass of the hot path: layout -> notify -> dispatch -> combine."""

@@ -100,8 +100,9 @@ moe_status moe_check_shape(const moe_shape* shape);
  * 14848 bytes for H = 7168 bf16. Returns -1 for H < 1. */
 int64_t moe_slot_stride(int32_t H, int32_t quant);
 
-/* Scratch bytes moe_layout and moe_notify need for this shape (the two calls
- * may share one buffer; its contents do not carry over between calls). */
+/* Scratch bytes moe_layout, moe_notify and moe_notify_expert need for this
+ * shape (the calls may share one buffer; its contents do not carry over
+ * between calls). */
 int64_t moe_scratch_bytes(const moe_shape* shape);
 
 /* Receive rows that always suffice when partitions are packed back to back
@@ -222,6 +223,54 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
                        const int64_t* part_row_base, int64_t arena_rows,
                        const int32_t* send_head, const int32_t* topk_idx,
                        const float* topk_weights, uint16_t* out, int32_t* err, void* stream);
+
+/*
+ * Expert-major receive layout ("HCCL Window 模式 (Non-SHMEM) 代码深度剖析",
+ * section 3.6 InputToShare and section 7.8 ReadBufferAndWeightedSum). Instead of
+ * one row per (token, destination rank), every valid (token, k) slot gets its
+ * own row, and rank d's partition holds its experts' rows expert by expert:
+ * local expert l starts at recv_expert_offset[d][l] (counts rounded up to
+ * expert_alignment; rows in the alignment gaps are not written), and inside an
+ * expert the slots are in (token, k) order. Each expert's rows are contiguous,
+ * ready for a grouped expert GEMM.
+ *
+ * moe_max_expert_rows: arena rows that always suffice: S*K + E*(expert_alignment-1).
+ *
+ * moe_notify_expert -- after moe_layout and moe_notify:
+ *   topk_idx                   int32 [S,K]
+ *   num_recv_tokens_per_expert int32 [P,E/P] and recv_expert_offset int32 [P,E/P] from moe_notify
+ *   slot_row                   int32 [S,K]   row of slot (g,k) inside rank (topk_idx/(E/P))'s
+ *                                            partition: recv_expert_offset[e] + the number of
+ *                                            earlier slots (token-major order) of expert e;
+ *                                            -1 for a masked or out-of-range slot
+ *   expert_part_base           int64 [P+1]   exclusive scan of the ranks' aligned row totals
+ *   scratch                    >= moe_scratch_bytes(shape) bytes, 256-byte aligned
+ *
+ * moe_dispatch_expert -- for every valid slot, row expert_part_base[d] + slot_row[g][k]
+ *   receives the payload (bf16, or int8 + scale, as moe_dispatch), the triple
+ *   (g / T, g % T, k), recv_src_idx[row] = g % T and recv_weight[row] =
+ *   topk_weights[g][k] (1 if topk_weights is NULL). Side arrays may be NULL.
+ *   Rows outside their partition or the arena are skipped (MOE_ERR_CAPACITY in err).
+ *
+ * moe_combine_expert --
+ *   out[g] = bf16_rne( sum over k ascending with a valid slot of
+ *                      w[g][k] * f32(y[expert_part_base[d] + slot_row[g][k]]) )
+ *   binary32 accumulator from +0, each product and sum rounded on its own, w = 1
+ *   when topk_weights is NULL. y rows are y_row_stride bytes apart.
+ */
+int64_t moe_max_expert_rows(const moe_shape* shape);
+moe_status moe_notify_expert(const moe_shape* shape, const int32_t* topk_idx,
+                             const int32_t* num_recv_tokens_per_expert, const int32_t* recv_expert_offset,
+                             int32_t* slot_row, int64_t* expert_part_base, void* scratch,
+                             int64_t scratch_bytes, void* stream);
+moe_status moe_dispatch_expert(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                               const float* topk_weights, const int32_t* slot_row,
+                               const int64_t* expert_part_base, void* recv_arena, int64_t arena_rows,
+                               int32_t* recv_src_idx, float* recv_weight, int32_t* err, void* stream);
+moe_status moe_combine_expert(const moe_shape* shape, const void* y, int64_t y_row_stride,
+                              const int64_t* expert_part_base, int64_t arena_rows, const int32_t* slot_row,
+                              const int32_t* topk_idx, const float* topk_weights, uint16_t* out,
+                              int32_t* err, void* stream);
 
 /*
  * moe_pad_partitions -- fixed-length receive partitions ("Ascend DeepEP MoE
