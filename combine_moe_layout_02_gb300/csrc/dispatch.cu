@@ -21,10 +21,12 @@
 //    cp.async.bulk.wait_group.read shows its stores have left shared memory.
 //    Warp 0 runs the copies; the other warps write the triples and side arrays
 //    for the same tokens in parallel.
-//  * int8: all warps read the row from the ring, reduce |x| to amax (warp
-//    shuffles + one shared slot per warp), quantise with IEEE division and
-//    round-half-even into a double-buffered shared int8 row, and the same bulk
-//    stores fan that row out to the destinations.
+//  * int8: a producer warp streams rows into the ring (full / empty
+//    mbarriers); consumer warps each take whole tokens: amax by a warp
+//    reduction, quantisation (exact round-half-even of x / scale, see
+//    quant_one) into the warp's own shared int8 row, then the same bulk stores
+//    fan that row out. A small ring and few consumers per CTA, so several CTAs
+//    (and producers) share an SM.
 // Every mbarrier wait is bounded; on time-out the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains its own copies (bounded) and returns.
 #include <cuda_bf16.h>
@@ -43,15 +45,28 @@
 #ifndef MOE_DISPATCH_STORE_DEPTH
 #define MOE_DISPATCH_STORE_DEPTH 1
 #endif
+// int8 dispatch: ring budget and number of quantising (consumer) warps per CTA.
+#ifndef MOE_DISPATCH_INT8_RING_BYTES
+#define MOE_DISPATCH_INT8_RING_BYTES (32 * 1024)
+#endif
+#ifndef MOE_DISPATCH_INT8_CONSUMERS
+#define MOE_DISPATCH_INT8_CONSUMERS 2
+#endif
 
 namespace moe {
 namespace {
 
 constexpr int kBf16Threads = 128;
-constexpr int kInt8Threads = 256;
+constexpr int kInt8Consumers = MOE_DISPATCH_INT8_CONSUMERS;
+constexpr int kInt8Threads = 32 * (1 + kInt8Consumers);
 constexpr int kMaxStages = MOE_DISPATCH_MAX_STAGES;
 constexpr int kStoreDepth = MOE_DISPATCH_STORE_DEPTH;
 static_assert(kStoreDepth >= 1 && kStoreDepth < kMaxStages, "store depth must leave a free slot");
+// The int8 ring has a multiple of kInt8Consumers slots, so a slot's successive
+// uses (tokens i and i + stages) belong to the same consumer warp: a warp only
+// ever waits on the phase after one it has already consumed, never two phases
+// ahead of the barrier.
+static_assert(kMaxStages >= kInt8Consumers, "the int8 ring needs a slot per consumer warp");
 
 struct DispatchSmem {
     size_t prb, bars, ring, qbuf, total;
@@ -62,9 +77,10 @@ __host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_
     DispatchSmem l;
     l.prb = 0;
     l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
-    l.ring = l.bars + static_cast<size_t>(round_up(kMaxStages * 8, 128));
+    // full[kMaxStages] then empty[kMaxStages] (the bf16 kernel uses full only)
+    l.ring = l.bars + static_cast<size_t>(round_up(2 * kMaxStages * 8, 128));
     l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
-    l.total = l.qbuf + (quant ? 2 * static_cast<size_t>(round_up(H, 128)) : 0);
+    l.total = l.qbuf + (quant ? kInt8Consumers * static_cast<size_t>(round_up(H, 128)) : 0);
     return l;
 }
 
@@ -262,99 +278,141 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-__device__ __forceinline__ uint32_t quant_pair(uint32_t v, float scale, bool zero) {
-    int32_t q0 = 0, q1 = 0;
-    if (!zero) {
-        q0 = __float2int_rn(__fdiv_rn(bf16_lo(v), scale));
-        q1 = __float2int_rn(__fdiv_rn(bf16_hi(v), scale));
-        q0 = max(-127, min(127, q0));
-        q1 = max(-127, min(127, q1));
-    }
-    return (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8);
+// q = rint(x / scale) with round-half-even, exactly as with IEEE division, for
+// finite x. The quotient is taken as t = x * r, r = 1 / scale rounded:
+// |t - x / scale| <= 127 * 2^-23 < 2^-15, so rounding t gives the same integer
+// unless t lies within 2^-15 of a half-integer; only then (or when r is not
+// finite) is the division done. |x / scale| <= 127 * (1 + 2^-23) < 127.5, so
+// q is already in [-127, 127] and needs no clamp.
+__device__ __forceinline__ int32_t quant_one(float x, float scale, float r, bool fast) {
+    const float t = __fmul_rn(x, r);
+    int32_t q = __float2int_rn(t);
+    if (!(fast && fabsf(t - __int2float_rn(q)) < 0.5f - 0x1p-15f)) q = __float2int_rn(__fdiv_rn(x, scale));
+    return q;
 }
 
+// 8 bf16 (one 16-byte chunk) -> 8 int8, packed little-endian.
+__device__ __forceinline__ uint2 quant_chunk(uint4 v, float scale, float r, bool fast, bool zero) {
+    if (zero) return make_uint2(0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int32_t q0 = quant_one(bf16_lo(w[2 * h]), scale, r, fast);
+        const int32_t q1 = quant_one(bf16_hi(w[2 * h]), scale, r, fast);
+        const int32_t q2 = quant_one(bf16_lo(w[2 * h + 1]), scale, r, fast);
+        const int32_t q3 = quant_one(bf16_hi(w[2 * h + 1]), scale, r, fast);
+        const uint32_t lo = __byte_perm(static_cast<uint32_t>(q0), static_cast<uint32_t>(q1), 0x0040);
+        const uint32_t hi = __byte_perm(static_cast<uint32_t>(q2), static_cast<uint32_t>(q3), 0x0040);
+        o[h] = __byte_perm(lo, hi, 0x5410);
+    }
+    return make_uint2(o[0], o[1]);
+}
+
+// max |x| over 8 bf16, as a bf16 pair (bf16 max is exact).
+__device__ __forceinline__ __nv_bfloat162 absmax_chunk(__nv_bfloat162 m, uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b;
+        memcpy(&b, &w[i], 4);
+        m = __hmax2(m, __habs2(b));
+    }
+    return m;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// int8 dispatch. Warp 0 is the producer: it streams source rows into the ring
+// (bulk loads completing on full[slot]) and reuses a slot once the consumer
+// that read it arrives on empty[slot]. Warps 1..kInt8Consumers each take
+// whole tokens in turn: amax by a warp reduction, scale = amax / 127, the
+// quantised row into the warp's own shared int8 row, then one bulk store per
+// destination, the scale block and the triple / side arrays. No block-wide
+// barrier on the token path.
 template <bool EXPERT>
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
     pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kInt8Threads / 32];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, true);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + kMaxStages;
     unsigned char* ring = smem + L.ring;
-    unsigned char* qbuf = smem + L.qbuf;
     const size_t qstride = static_cast<size_t>(round_up(a.H, 128));
-    load_prb_and_init(a, prb, bars);
+    for (int i = threadIdx.x; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < a.stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
     const int64_t n_local = blockIdx.x < a.S ? (a.S - 1 - blockIdx.x) / G + 1 : 0;
     const int NS = a.stages;
     const uint32_t RB = a.row_bytes;
-    const int nchunks = a.H / 8;  // 16-byte chunks of the bf16 row
 
-    int64_t last_issued = -1;
-    if (tid == 0) {
-        const int64_t npro = n_local < NS ? n_local : NS;
-        for (int64_t i = 0; i < npro; ++i) {
-            mbar_arrive_expect_tx(&bars[i], RB);
-            bulk_load(ring + i * RB, a.x + (blockIdx.x + i * G) * a.H, RB, &bars[i]);
+    if (warp == 0) {
+        if (lane != 0) return;
+        int64_t issued = 0;
+        bool failed = false;
+        for (; issued < n_local; ++issued) {
+            const int slot = static_cast<int>(issued % NS);
+            if (issued >= NS && !mbar_wait(&empty[slot], static_cast<uint32_t>(((issued / NS) - 1) & 1))) {
+                failed = true;
+                break;
+            }
+            mbar_arrive_expect_tx(&full[slot], RB);
+            bulk_load(ring + static_cast<size_t>(slot) * RB, a.x + (blockIdx.x + issued * G) * a.H, RB,
+                      &full[slot]);
         }
-        last_issued = npro - 1;
+        if (failed) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+        // Loads still in flight land before the CTA may exit.
+        const int64_t first = issued > NS ? issued - NS : 0;
+        drain_loads(full, NS, first, issued - 1);
+        return;
     }
-    bool failed = false;
-    int64_t i = 0;
-    for (; i < n_local; ++i) {
+
+    const int cw = warp - 1;
+    unsigned char* q = smem + L.qbuf + static_cast<size_t>(cw) * qstride;
+    const int nchunks = a.H / 8;
+    for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
-        const bool ok = mbar_wait(&bars[slot], static_cast<uint32_t>((i / NS) & 1));
-        if (__syncthreads_or(!ok)) {
-            failed = true;
+        const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>((i / NS) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
             break;
         }
         const uint4* row = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * RB);
-        float m = 0.f;
-        for (int j = tid; j < nchunks; j += nthreads) {
-            const uint4 v = row[j];
-            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))));
-            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
-            m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
-        }
+        __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+        for (int j = lane; j < nchunks; j += 32) m2 = absmax_chunk(m2, row[j]);
+        float m = fmaxf(__bfloat162float(m2.x), __bfloat162float(m2.y));
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        float amax = 0.f;
-        for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, red[w]);
-        const float scale = __fdiv_rn(amax, 127.0f);
-        const bool zero = amax == 0.f;
-        unsigned char* q = qbuf + static_cast<size_t>(i & 1) * qstride;
-        for (int j = tid; j < nchunks; j += nthreads) {
-            const uint4 v = row[j];
-            uint2 packed;
-            packed.x = quant_pair(v.x, scale, zero) | (quant_pair(v.y, scale, zero) << 16);
-            packed.y = quant_pair(v.z, scale, zero) | (quant_pair(v.w, scale, zero) << 16);
-            reinterpret_cast<uint2*>(q)[j] = packed;
-        }
+        const float scale = __fdiv_rn(m, 127.0f);
+        const bool zero = m == 0.f;
+        const float r = zero ? 0.f : __frcp_rn(scale);
+        const bool fast = !zero && isfinite(r);
+        // This warp's previous stores must have finished reading q.
+        bulk_wait_read<0>();
+        __syncwarp();
+        for (int j = lane; j < nchunks; j += 32)
+            reinterpret_cast<uint2*>(q)[j] = quant_chunk(row[j], scale, r, fast, zero);
         fence_proxy_async_smem();
-        __syncthreads();
-        // The ring slot has been read by every thread: refill it.
-        if (tid == 0) {
-            const int64_t nxt = i + NS;
-            if (nxt < n_local) {
-                mbar_arrive_expect_tx(&bars[slot], RB);
-                bulk_load(ring + static_cast<size_t>(slot) * RB, a.x + (blockIdx.x + nxt * G) * a.H, RB,
-                          &bars[slot]);
-                last_issued = nxt;
-            }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // ring slot read by every lane
         const int nfan = EXPERT ? a.K : a.P;
-        for (int d = tid; d < nfan; d += nthreads) {
+        for (int d = lane; d < nfan; d += 32) {
             uint8_t* dst = nullptr;
             if constexpr (EXPERT) {
-                int64_t row;
-                dst = expert_slot_of(a, prb, g, d, &row);
+                int64_t rowi;
+                dst = expert_slot_of(a, prb, g, d, &rowi);
             } else {
                 const int32_t sh = __ldg(a.send_head + g * a.P + d);
                 if (sh >= 0) dst = slot_of(a, prb, d, sh);
@@ -368,21 +426,12 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
             }
         }
         bulk_commit();
-        if (warp == static_cast<int>(i % nwarps)) {
-            if constexpr (EXPERT)
-                write_slot_meta(a, prb, g, lane);
-            else
-                write_token_meta(a, prb, g, lane);
-        }
-        // The int8 buffer written two tokens from now is this token's partner:
-        // its stores must have left shared memory before then.
-        bulk_wait_read<1>();
+        if constexpr (EXPERT)
+            write_slot_meta(a, prb, g, lane);
+        else
+            write_token_meta(a, prb, g, lane);
     }
     bulk_wait<0>();
-    if (failed && tid == 0) {
-        raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
-        drain_loads(bars, NS, i, last_issued);
-    }
 }
 
 }  // namespace
@@ -393,11 +442,24 @@ cudaError_t launch_dispatch_mode(const moe_shape& s, DispatchArgs a, cudaStream_
     const bool quant = s.quant != 0;
     // Ring depth: as many rows as fit in the ring budget, at least one more
     // than the store depth (and 2), at most kMaxStages.
-    int stages = static_cast<int>(MOE_DISPATCH_RING_BYTES / a.row_bytes);
-    const int min_stages = kStoreDepth + 1 > 2 ? kStoreDepth + 1 : 2;
-    stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
+    int stages;
+    if (quant) {
+        // A multiple of the consumer count (see kInt8Consumers), at least one
+        // slot per consumer, at most kMaxStages.
+        const int per = static_cast<int>(MOE_DISPATCH_INT8_RING_BYTES / (a.row_bytes * kInt8Consumers));
+        const int groups_max = kMaxStages / kInt8Consumers;
+        stages = kInt8Consumers * (per < 1 ? 1 : (per > groups_max ? groups_max : per));
+    } else {
+        stages = static_cast<int>(MOE_DISPATCH_RING_BYTES / a.row_bytes);
+        const int min_stages = kStoreDepth + 1 > 2 ? kStoreDepth + 1 : 2;
+        stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
+    }
     a.stages = stages;
     const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
+    int max_smem = 0;
+    cudaError_t e0 = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, 0);
+    if (e0 != cudaSuccess) return e0;
+    if (L.total > static_cast<size_t>(max_smem)) return cudaErrorInvalidConfiguration;
     const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel<EXPERT>)
                            : reinterpret_cast<const void*>(dispatch_bf16_kernel<EXPERT>);
     const int threads = quant ? kInt8Threads : kBf16Threads;

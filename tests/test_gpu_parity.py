@@ -255,3 +255,30 @@ def test_fixed_capacity_with_padding(quant):
                                       ref["arena"][:, scale_off:scale_off + 4])
     for k in ("recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
         np.testing.assert_array_equal(getattr(buf, k).cpu().numpy(), ref[k], err_msg=k)
+
+
+def test_int8_exact_ties_take_the_division_path():
+    """Rows whose quotients x / scale are exact half-integers (scale = 1 and
+    scale = 1/8): round-half-even must match the oracle's IEEE division bit
+    for bit, also when the quotient is reached through the reciprocal."""
+    w = inputs.make(2, 4, 8, 256, 2, seed=31)
+    f = np.zeros((w.S, w.H), np.float32)
+    ks = np.arange(-127, 127, dtype=np.float32)
+    f[0, :ks.shape[0]] = ks + 0.5          # ties at scale 1 (amax 127 set below)
+    f[0, -1] = 127.0
+    f[1, :ks.shape[0]] = (2 * ks + 1) / 16  # ties at scale 1/8 (amax 15.875)
+    f[1, -1] = -15.875
+    rng = np.random.default_rng(4)
+    # Odd multiples of 1/16 (bf16-exact); rows whose amax is 15.875 tie exactly.
+    f[2:] = ((2 * rng.integers(-127, 127, size=(w.S - 2, w.H)) + 1) / 16).astype(np.float32)
+    w.x_bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert ((w.x_bits.astype(np.uint32) << 16).view(np.float32) == f).all()
+    _check_all(w, quant=1, y_mode="int8expert")
+
+
+@pytest.mark.parametrize("H", [16384, 1024])
+def test_int8_ring_depths(H):
+    """int8 dispatch with 32 KB rows (ring of one slot per consumer warp) and
+    2 KB rows (two slots per consumer warp)."""
+    w = inputs.make(4, 16, 40, H, 3, seed=H % 97, mask_frac=0.1)
+    _check_all(w, quant=1, y_mode="int8expert")
