@@ -304,19 +304,27 @@ def run_ours(args, world, rank, local):
         y_out = y_out.view(torch.int16)
         y_stride = 2 * w.H
 
+    fused = args.fused
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        buf.layout(idx, stream)
-        buf.notify(stream)
-        if expert:
-            buf.notify_expert(idx, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        if expert:
-            buf.dispatch_expert(x, idx, wts, stream)
+        if fused:
+            # layout + notify + dispatch in one launch: timed as "dispatch"
+            if ev is not None:
+                ev[1].record(stream)
+            buf.dispatch_fused(x, idx, wts, stream)
         else:
-            buf.dispatch(x, idx, wts, stream)
+            buf.layout(idx, stream)
+            buf.notify(stream)
+            if expert:
+                buf.notify_expert(idx, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            if expert:
+                buf.dispatch_expert(x, idx, wts, stream)
+            else:
+                buf.dispatch(x, idx, wts, stream)
         if ev is not None:
             ev[2].record(stream)
         if expert:
@@ -412,8 +420,9 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout),
-        "gpu_launches": (9 if expert else 6) * args.steps,
+        "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
+                       fused=bool(args.fused)),
+        "gpu_launches": (2 if args.fused else (9 if expert else 6)) * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "traffic": recorded_traffic(args.workload, kname),
@@ -447,6 +456,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
                     help="receive layout: one row per (token, rank), or one per (token, k) grouped by expert")
+    ap.add_argument("--fused", action="store_true",
+                    help="layout + notify + dispatch as one cooperative launch (small shapes)")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="override T (a smaller case of the same workload, e.g. for profiling)")
     ap.add_argument("--ref-tokens", type=int, default=512,

@@ -81,8 +81,10 @@ int64_t moe_scratch_bytes(const moe_shape* s) {
     const int64_t a = layout_plan(*s).scratch_bytes;
     const int64_t b = notify_scratch_bytes(*s);
     const int64_t c = notify_expert_scratch_bytes(*s);
+    const int64_t f = fused_supported(*s) ? fused_scratch_bytes(*s) : 0;
     int64_t m = a > b ? a : b;
     m = m > c ? m : c;
+    m = m > f ? m : f;
     return m > 256 ? m : 256;
 }
 
@@ -214,6 +216,64 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
     a.out = out;
     a.err = err;
     return from_cuda(launch_combine(s, a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_fused(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                              const float* topk_weights, int32_t* num_tokens_per_rank,
+                              int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                              uint32_t* is_token_in_rank_bits, int32_t* rank_prefix_matrix,
+                              int32_t* channel_prefix_matrix, int32_t* recv_channel_prefix_matrix,
+                              int32_t* num_recv_tokens, int32_t* num_recv_tokens_per_expert,
+                              int32_t* recv_expert_offset, int32_t* send_head, int64_t* part_row_base,
+                              void* recv_arena, int64_t arena_rows, int32_t* recv_src_idx,
+                              int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* err, void* scratch,
+                              int64_t scratch_bytes, void* stream) {
+    moe_status st = moe_check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!fused_supported(s)) return MOE_ERR_UNSUPPORTED;
+    const int64_t S = s.S;
+    if (arena_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(x, S * s.H, 16) || !ok_ptr(topk_idx, S * s.K, 16) || !ok_opt(topk_weights, 16) ||
+        !ok_ptr(num_tokens_per_rank, 1, 16) || !ok_ptr(num_tokens_per_expert, 1, 16) ||
+        !ok_ptr(is_token_in_rank, S * s.P, 16) || !ok_opt(is_token_in_rank_bits, 16) ||
+        !ok_ptr(rank_prefix_matrix, 1, 16) || !ok_ptr(channel_prefix_matrix, 1, 16) ||
+        !ok_ptr(recv_channel_prefix_matrix, 1, 16) || !ok_ptr(num_recv_tokens, 1, 16) ||
+        !ok_ptr(num_recv_tokens_per_expert, 1, 16) || !ok_ptr(recv_expert_offset, 1, 16) ||
+        !ok_ptr(send_head, S * s.P, 16) || !ok_ptr(part_row_base, 1, 16) || !ok_ptr(recv_arena, arena_rows, 16) ||
+        !ok_opt(recv_src_idx, 16) || !ok_opt(recv_topk_idx, 16) || !ok_opt(recv_topk_weights, 16) ||
+        !ok_opt(err, 4) || !ok_ptr(scratch, 1, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (recv_topk_weights && !topk_weights && S > 0) return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_scratch_bytes(shape)) return MOE_ERR_INVALID_ARG;
+    DispatchArgs a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.K = s.K;
+    a.H = s.H;
+    a.epr = s.E / s.P;
+    a.S = S;
+    a.T = S / s.P;
+    a.x = x;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.send_head = send_head;
+    a.part_row_base = part_row_base;
+    a.arena = static_cast<uint8_t*>(recv_arena);
+    a.arena_rows = arena_rows;
+    a.stride = moe_slot_stride(s.H, 0);
+    a.scale_off = round_up(static_cast<int64_t>(s.H) * 2, 32);
+    a.triple_off = a.scale_off + 32;
+    a.recv_src_idx = recv_src_idx;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_weights = recv_topk_weights;
+    a.err = err;
+    a.row_bytes = static_cast<uint32_t>(s.H) * 2u;
+    return from_cuda(launch_fused(s, x, topk_idx, topk_weights, num_tokens_per_rank, num_tokens_per_expert,
+                                  is_token_in_rank, is_token_in_rank_bits, rank_prefix_matrix,
+                                  channel_prefix_matrix, recv_channel_prefix_matrix, num_recv_tokens,
+                                  num_recv_tokens_per_expert, recv_expert_offset, send_head, part_row_base, a,
+                                  err, scratch, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_notify_expert(const moe_shape* shape, const int32_t* topk_idx,

@@ -216,6 +216,14 @@ cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* pr
                        int64_t arena_rows, int32_t* src_idx, int32_t* tk_idx, float* tk_w,
                        cudaStream_t stream);
 
+bool fused_supported(const moe_shape& s);
+int64_t fused_scratch_bytes(const moe_shape& s);
+cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* topk_idx, const float* topk_weights,
+                         int32_t* ntpr, int32_t* ntpe, uint8_t* itr, uint32_t* bits, int32_t* rpm, int32_t* cpm,
+                         int32_t* rcpm, int32_t* nrt, int32_t* nrtpe, int32_t* reo, int32_t* send_head,
+                         int64_t* part_row_base, const DispatchArgs& d, int32_t* err, void* scratch,
+                         cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -26,7 +26,7 @@ MOE_ERR_INCONSISTENT = 7
 EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
            "moe_layout_static_scratch", "moe_pad_partitions", "moe_max_expert_rows",
-           "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert")
+           "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused")
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
 MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_combine.argtypes = [sp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_fused.restype = i32
+    L.moe_dispatch_fused.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, i64, vp, vp, vp, vp, vp, i64, vp]
     L.moe_max_expert_rows.restype = i64
     L.moe_max_expert_rows.argtypes = [sp]
     L.moe_notify_expert.restype = i32
@@ -188,6 +191,22 @@ def moe_combine(shape, y, y_row_stride, part_row_base, arena_rows, send_head, to
                            int(arena_rows), _ptr(send_head), _ptr(topk_idx), _ptr(topk_weights),
                            _ptr(out), _ptr(err), _stream(stream))
     _check(st, "moe_combine")
+
+
+def moe_dispatch_fused(shape, x, topk_idx, topk_weights, num_tokens_per_rank, num_tokens_per_expert,
+                       is_token_in_rank, is_token_in_rank_bits, rank_prefix_matrix, channel_prefix_matrix,
+                       recv_channel_prefix_matrix, num_recv_tokens, num_recv_tokens_per_expert,
+                       recv_expert_offset, send_head, part_row_base, recv_arena, arena_rows, recv_src_idx,
+                       recv_topk_idx, recv_topk_weights, err, scratch, stream=None):
+    st = lib().moe_dispatch_fused(
+        ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(topk_weights), _ptr(num_tokens_per_rank),
+        _ptr(num_tokens_per_expert), _ptr(is_token_in_rank), _ptr(is_token_in_rank_bits),
+        _ptr(rank_prefix_matrix), _ptr(channel_prefix_matrix), _ptr(recv_channel_prefix_matrix),
+        _ptr(num_recv_tokens), _ptr(num_recv_tokens_per_expert), _ptr(recv_expert_offset), _ptr(send_head),
+        _ptr(part_row_base), _ptr(recv_arena), int(arena_rows), _ptr(recv_src_idx), _ptr(recv_topk_idx),
+        _ptr(recv_topk_weights), _ptr(err), _ptr(scratch), int(scratch.numel() * scratch.element_size()),
+        _stream(stream))
+    _check(st, "moe_dispatch_fused")
 
 
 def moe_max_expert_rows(shape: moe_shape) -> int:
@@ -342,6 +361,16 @@ class Buffers:
             y, y_row_stride = self.expert_arena, self.stride
         moe_combine_expert(self.shape, y, y_row_stride, self.expert_part_base, self.expert_rows,
                            self.slot_row, topk_idx, topk_weights, out, self.err, stream)
+
+    def dispatch_fused(self, x, topk_idx, topk_weights, stream=None):
+        """layout + notify + dispatch in one launch (small shapes only)."""
+        moe_dispatch_fused(self.shape, x, topk_idx, topk_weights, self.num_tokens_per_rank,
+                           self.num_tokens_per_expert, self.is_token_in_rank, self.is_token_in_rank_bits,
+                           self.rank_prefix_matrix, self.channel_prefix_matrix,
+                           self.recv_channel_prefix_matrix, self.num_recv_tokens,
+                           self.num_recv_tokens_per_expert, self.recv_expert_offset, self.send_head,
+                           self.part_row_base, self.recv_arena, self.arena_rows, self.recv_src_idx,
+                           self.recv_topk_idx, self.recv_topk_weights, self.err, self.scratch, stream)
 
     def step(self, x, topk_idx, topk_weights, out, stream=None):
         """One pass of the hot path: layout -> notify -> dispatch -> combine."""

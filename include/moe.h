@@ -100,9 +100,9 @@ moe_status moe_check_shape(const moe_shape* shape);
  * 14848 bytes for H = 7168 bf16. Returns -1 for H < 1. */
 int64_t moe_slot_stride(int32_t H, int32_t quant);
 
-/* Scratch bytes moe_layout, moe_notify and moe_notify_expert need for this
- * shape (the calls may share one buffer; its contents do not carry over
- * between calls). */
+/* Scratch bytes moe_layout, moe_notify, moe_notify_expert and
+ * moe_dispatch_fused need for this shape (the calls may share one buffer; its
+ * contents do not carry over between calls). */
 int64_t moe_scratch_bytes(const moe_shape* shape);
 
 /* Receive rows that always suffice when partitions are packed back to back
@@ -223,6 +223,33 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
                        const int64_t* part_row_base, int64_t arena_rows,
                        const int32_t* send_head, const int32_t* topk_idx,
                        const float* topk_weights, uint16_t* out, int32_t* err, void* stream);
+
+/*
+ * moe_dispatch_fused -- moe_layout + moe_notify + moe_dispatch in one launch,
+ * for the small-message regime where the fixed cost of the routing tables
+ * dominates the payload ("Ascend DeepEP MoE Dispatch Optimization", section
+ * "128P 为什么会放大问题"; the single-kernel counting + prefix + copy shape of
+ * "DeepEP Warp Specialization 深度分析", dispatch_impl). Every output has the
+ * meaning, layout and value of the three separate calls with packed partitions
+ * (part_row_base is written here and used for the rows).
+ *
+ * One cooperative persistent kernel (one CTA per SM) with two bounded grid
+ * barriers; the barrier counter lives in scratch and is zeroed on the stream
+ * before the launch, as is `err` (then raised to MOE_ERR_TOPK_OUT_OF_RANGE,
+ * MOE_ERR_CAPACITY or MOE_ERR_DEVICE_TIMEOUT if needed).
+ * Supported: P <= 64, E <= 1024, H <= 8192, quant = 0; other shapes return
+ * MOE_ERR_UNSUPPORTED (use the separate calls). scratch >= moe_scratch_bytes.
+ */
+moe_status moe_dispatch_fused(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
+                              const float* topk_weights, int32_t* num_tokens_per_rank,
+                              int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                              uint32_t* is_token_in_rank_bits, int32_t* rank_prefix_matrix,
+                              int32_t* channel_prefix_matrix, int32_t* recv_channel_prefix_matrix,
+                              int32_t* num_recv_tokens, int32_t* num_recv_tokens_per_expert,
+                              int32_t* recv_expert_offset, int32_t* send_head, int64_t* part_row_base,
+                              void* recv_arena, int64_t arena_rows, int32_t* recv_src_idx,
+                              int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* err, void* scratch,
+                              int64_t scratch_bytes, void* stream);
 
 /*
  * Expert-major receive layout ("HCCL Window 模式 (Non-SHMEM) 代码深度剖析",
