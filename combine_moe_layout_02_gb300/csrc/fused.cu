@@ -9,26 +9,44 @@
 // bounded grid barriers instead of inter-GPU signals. Outputs are exactly
 // those of moe_layout, moe_notify and moe_dispatch with packed partitions.
 //
-// Phase A (one warp per (source rank, channel)): distinct ranks per token from
-//   topk_idx; is_token_in_rank rows (+ bits); per-channel rank counts (ballots)
-//   and expert counts (__match_any_sync leaders into warp-private shared
-//   counters) into scratch.
-// grid barrier
-// Phase B: every CTA rebuilds, in shared memory, the per-source rank counts
-//   and their running sum over sources from the channel counts (a few KB for
-//   the supported P); CTA 0 writes num_tokens_per_rank, rank_prefix_matrix,
-//   num_recv_tokens and part_row_base. Expert tables are spread over all
-//   threads. Then one warp per channel writes channel_prefix_matrix,
-//   recv_channel_prefix_matrix and the channel's send_head rows.
-// grid barrier
-// Phase C (one warp per token, all warps of the grid): each warp bulk-loads
-//   its token's row into its shared-memory buffer (mbarrier), its lanes
-//   bulk-store it to every destination, and the warp writes the triple and
-//   side arrays.
+// The control phases are laid out so that no warp waits on a chain of
+// dependent global loads: every count a later phase needs is written where
+// that phase reads it contiguously, and loads are issued in batches.
 //
-// Supported: P <= 64, E <= 1024, H <= 8192; larger shapes use the separate
-// calls. The grid barrier counter lives in scratch and is zeroed on the
-// stream before the launch.
+// Start: each warp issues the bulk loads of its first token rows into its
+//   own ring of row buffers (x is an input, so the copies need no barrier).
+// Phase A (one warp per channel ch = (source rank s, channel c)): for 32
+//   tokens at a time (one per lane), the destination-rank mask of each token
+//   (topk_idx) and the expert counts (shared-memory integer atomics);
+//   is_token_in_rank rows (+ bits); then, lanes over destination ranks, the
+//   position of each token among the channel's tokens sent to each rank,
+//   written to send_head (local positions, made global in phase C); the
+//   channel's rank counts go to ccT[d][ch] (rank-major, so phase B scans a
+//   contiguous column) and its expert counts to ecount[ch][e].
+// grid barrier
+// Phase B (one warp per task): destination rank d scans column ccT[d][.] over
+//   the flattened (s, c) order: the exclusive prefix is the channel's first
+//   row on d, which is recv_channel_prefix_matrix and the base of send_head
+//   ("internode.cu", notify: prefix sums over (source, channel)); the same
+//   column gives channel_prefix_matrix, num_tokens_per_rank,
+//   rank_prefix_matrix and num_recv_tokens. Expert e sums its channel counts
+//   per source (num_tokens_per_expert) and in total (aligned: the receive
+//   counts per expert).
+// grid barrier
+// Phase C: every CTA scans num_recv_tokens into part_row_base (shared
+//   memory); one warp per rank scans its experts' aligned counts into
+//   recv_expert_offset; then one warp per token stream: send_head entries
+//   become global rows (local position + the channel's first row,
+//   recv_channel_prefix_matrix[d][s][c]), one lane per destination
+//   bulk-stores the row from the ring, the warp writes the triple and side
+//   arrays and refills the ring. The routing of the next token is loaded
+//   while the current one is copied.
+//
+// Supported: P <= 64, E <= 1024, H <= 8192, K <= 16, P * num_channels <=
+// 4096, bf16; larger shapes use the separate calls. The grid barrier counter
+// lives in scratch and is zeroed by a one-thread kernel launched just before
+// (both launches use programmatic dependent launch, so the fused kernel is
+// scheduled while earlier work drains); err is cleared by the kernel itself.
 #include "moe_device.cuh"
 
 namespace moe {
@@ -39,10 +57,21 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxP = 64;
 constexpr int kMaxE = 1024;
 constexpr int kMaxH = 8192;
+constexpr int kMaxPC = 4096;  // P * num_channels (per-warp column in shared memory)
+constexpr int kMaxK = 16;
+constexpr int kMaxNB = 4;     // row buffers per warp
+constexpr int kBarBytes = kWarps * kMaxNB * 8;
+constexpr int kSeg = 16;      // column elements per lane per block in phase B
+constexpr int kSumUnroll = 16;
+// Dynamic shared memory a CTA may use next to the kernel's static shared
+// memory (sm_100-class opt-in limit 227 KB, less a margin for static data).
+constexpr int kSmemBudget = 227 * 1024 - 1024;
 
 struct FusedArgs {
-    int32_t P, E, K, H, C, A, epr;
-    int64_t S, T;
+    int32_t P, E, K, H, C, A, epr, nb;
+    uint32_t cq, cr;        // T = cq * C + cr: channels c < cr hold cq + 1 tokens, the rest cq
+    int64_t S, T, PC, PCp;
+    uint32_t ab_off;        // byte offset of the phase A / B region in dynamic shared memory
     const uint16_t* x;
     const int32_t* topk_idx;
     const float* topk_weights;
@@ -58,9 +87,9 @@ struct FusedArgs {
     int32_t* reo;
     int32_t* send_head;
     int64_t* part_row_base;
-    DispatchArgs d;       // payload stage (part_row_base, send_head as above)
-    int32_t* ccount;      // scratch [P*C][P]
-    int32_t* ecount;      // scratch [P*C][E]
+    DispatchArgs d;         // payload stage (part_row_base, send_head as above)
+    int32_t* ccT;           // scratch [P][PCp]: tokens of channel ch sent to rank d
+    int32_t* ecount;        // scratch [P*C][E]: slots of channel ch on expert e
     unsigned int* barrier;  // scratch, zeroed before launch
     int32_t* err;
 };
@@ -90,227 +119,342 @@ __device__ bool grid_barrier(unsigned int* counter, unsigned int target, int32_t
     return ok != 0;
 }
 
-// ---- phase A: counts and the token -> rank table -------------------------------
-__device__ void phase_counts(const FusedArgs& a, unsigned char* smem) {
+__device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+// 4 mask bits -> 4 bytes of 0 / 1 (little-endian).
+__device__ __forceinline__ uint32_t bytes_of_bits(uint32_t nib) {
+    return (nib & 1u) | ((nib & 2u) << 7) | ((nib & 4u) << 14) | ((nib & 8u) << 21);
+}
+
+// is_token_in_rank row of one token from its rank mask.
+__device__ __forceinline__ void write_itr_row(uint8_t* row, uint64_t mask, int P) {
+    if ((P & 15) == 0) {
+        for (int q = 0; q < P; q += 16) {
+            const uint32_t m16 = static_cast<uint32_t>(mask >> q);
+            *reinterpret_cast<uint4*>(row + q) =
+                make_uint4(bytes_of_bits(m16 & 15u), bytes_of_bits((m16 >> 4) & 15u),
+                           bytes_of_bits((m16 >> 8) & 15u), bytes_of_bits((m16 >> 12) & 15u));
+        }
+    } else if ((P & 3) == 0) {
+        for (int q = 0; q < P; q += 4)
+            *reinterpret_cast<uint32_t*>(row + q) = bytes_of_bits(static_cast<uint32_t>(mask >> q) & 15u);
+    } else {
+        for (int q = 0; q < P; ++q) row[q] = static_cast<uint8_t>((mask >> q) & 1ull);
+    }
+}
+
+// ---- phase A: masks, local positions, channel counts ------------------------------
+// Returns true if this thread saw an expert id >= E.
+__device__ bool phase_counts(const FusedArgs& a, int32_t* region) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* hist_e = reinterpret_cast<int32_t*>(smem) + warp * (a.E + a.P);
-    int32_t* hist_r = hist_e + a.E;
-    const int64_t chans = static_cast<int64_t>(a.P) * a.C;
+    const int P = a.P, E = a.E, K = a.K;
+    int32_t* hist = region + warp * E;
     const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
-    const int W = (a.P + 31) / 32;
-    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * kWarps + warp; ch < chans; ch += total_warps) {
-        const int64_t s = ch / a.C, c = ch % a.C;
+    const int W = (P + 31) / 32;
+    bool bad = false;
+    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * kWarps + warp; ch < a.PC; ch += total_warps) {
+        const uint32_t s32 = static_cast<uint32_t>(ch) / static_cast<uint32_t>(a.C);
+        const int64_t s = s32, c = ch - static_cast<int64_t>(s32) * a.C;
         int64_t b, e;
         split_range(a.T, a.C, c, &b, &e);
-        for (int i = lane; i < a.E + a.P; i += 32) hist_e[i] = 0;
+        for (int i = lane; i < E; i += 32) hist[i] = 0;
         __syncwarp();
+        int32_t cnt0 = 0, cnt1 = 0;  // this channel's tokens sent to rank lane / lane + 32
         for (int64_t t0 = b; t0 < e; t0 += 32) {
             const int64_t t = t0 + lane;
             const bool active = t < e;
             const int64_t g = s * a.T + t;
+            int32_t ids[kMaxK];
+#pragma unroll
+            for (int k = 0; k < kMaxK; ++k) ids[k] = (k < K && active) ? __ldg(a.topk_idx + g * K + k) : -1;
             uint64_t mask = 0;
-            for (int k = 0; k < a.K; ++k) {
-                int32_t ex = active ? __ldg(a.topk_idx + g * a.K + k) : -1;
-                if (ex >= a.E) {
-                    raise_error(a.err, MOE_ERR_TOPK_OUT_OF_RANGE);
-                    ex = -1;
+#pragma unroll
+            for (int k = 0; k < kMaxK; ++k) {
+                if (k < K) {
+                    const int32_t ex = ids[k];
+                    if (ex >= E) bad = true;
+                    if (ex >= 0 && ex < E) {
+                        atomicAdd(hist + ex, 1);  // integer counts: the order does not matter
+                        mask |= 1ull << (ex / a.epr);
+                    }
                 }
-                if (ex < 0) ex = -1;
-                const uint32_t grp = __match_any_sync(0xffffffffu, ex);
-                if (ex >= 0) {
-                    if (lane == __ffs(grp) - 1) hist_e[ex] += __popc(grp);
-                    mask |= 1ull << (ex / a.epr);
-                }
-                __syncwarp();
             }
             if (active) {
-                uint8_t* row = a.itr + g * a.P;
-                for (int d = 0; d < a.P; ++d) row[d] = static_cast<uint8_t>((mask >> d) & 1ull);
-                if (a.bits) {
+                write_itr_row(a.itr + g * P, mask, P);
+                if (a.bits)
                     for (int w = 0; w < W; ++w) a.bits[g * W + w] = static_cast<uint32_t>(mask >> (32 * w));
+            }
+            // Lanes over destinations: tokens of this step in order, so each
+            // lane's running count is the token's position on its rank.
+            const int m = e - t0 < 32 ? static_cast<int>(e - t0) : 32;
+            int32_t* row = a.send_head + (s * a.T + t0) * P;
+            for (int j = 0; j < m; ++j, row += P) {
+                const unsigned long long mj = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(mask), j);
+                const int32_t h0 = static_cast<int32_t>((mj >> lane) & 1ull);
+                if (lane < P) row[lane] = h0 ? cnt0 : -1;
+                cnt0 += h0;
+                if (P > 32) {
+                    const int32_t h1 = static_cast<int32_t>((mj >> (lane + 32)) & 1ull);
+                    if (lane + 32 < P) row[lane + 32] = h1 ? cnt1 : -1;
+                    cnt1 += h1;
                 }
             }
-            for (int d = 0; d < a.P; ++d) {
-                const uint32_t bal = __ballot_sync(0xffffffffu, (mask >> d) & 1ull);
-                if (lane == (d & 31)) hist_r[d] += __popc(bal);
-            }
-            __syncwarp();
         }
-        for (int d = lane; d < a.P; d += 32) a.ccount[ch * a.P + d] = hist_r[d];
-        for (int x = lane; x < a.E; x += 32) a.ecount[ch * a.E + x] = hist_e[x];
+        if (lane < P) a.ccT[lane * a.PCp + ch] = cnt0;
+        if (lane + 32 < P) a.ccT[(lane + 32) * a.PCp + ch] = cnt1;
+        __syncwarp();
+        for (int x = lane; x < E; x += 32) a.ecount[ch * E + x] = hist[x];
         __syncwarp();
     }
+    return bad;
 }
 
-// ---- phase B: tables and send_head -------------------------------------------
-__device__ void phase_tables(const FusedArgs& a, unsigned char* smem) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int P = a.P, C = a.C, E = a.E;
-    int32_t* tot = reinterpret_cast<int32_t*>(smem);  // [P][P] per-source rank counts
-    int32_t* run = tot + P * P;                        // [P][P] inclusive over sources
-    int64_t* prb = reinterpret_cast<int64_t*>(run + P * P);  // [P+1]
-    for (int i = tid; i < P * P; i += kThreads) {
-        const int s = i / P, d = i % P;
+// ---- phase B: column scans (ranks) and expert sums ----------------------------------
+// Skewed index into a warp's column copy: lane-contiguous runs of kSeg words
+// fall in distinct banks.
+__device__ __forceinline__ int64_t cx(int64_t j) { return j + (j >> 4); }
+
+__device__ void scan_rank_column(const FusedArgs& a, int d, int32_t* colx, int lane) {
+    const int P = a.P, C = a.C;
+    const int64_t PC = a.PC;
+    const int32_t* src = a.ccT + d * a.PCp;
+    int32_t* rc = a.rcpm + d * PC;  // [d][s][c] with j = s * C + c
+    int32_t carry = 0;
+    for (int64_t j0 = 0; j0 < PC; j0 += 32 * kSeg) {
+        const int64_t jb = j0 + static_cast<int64_t>(lane) * kSeg;
+        int32_t v[kSeg];
+#pragma unroll
+        for (int q = 0; q < kSeg; q += 4) {
+            // jb + q is a multiple of 4 and the row stride PCp too: whole int4 in the row.
+            const int4 u = jb + q < a.PCp ? __ldcg(reinterpret_cast<const int4*>(src + jb + q)) : make_int4(0, 0, 0, 0);
+            v[q] = u.x;
+            v[q + 1] = u.y;
+            v[q + 2] = u.z;
+            v[q + 3] = u.w;
+        }
         int32_t sum = 0;
-        for (int c = 0; c < C; ++c) sum += __ldcg(a.ccount + (static_cast<int64_t>(s) * C + c) * P + d);
-        tot[i] = sum;
-    }
-    __syncthreads();
-    for (int d = tid; d < P; d += kThreads) {
-        int32_t r = 0;
-        for (int s = 0; s < P; ++s) {
-            r += tot[s * P + d];
-            run[s * P + d] = r;
+#pragma unroll
+        for (int u = 0; u < kSeg; ++u) {
+            if (jb + u >= PC) v[u] = 0;  // row padding
+            sum += v[u];
         }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int64_t acc = 0;
-        for (int d = 0; d < P; ++d) {
-            prb[d] = acc;
-            acc += run[(P - 1) * P + d];
-        }
-        prb[P] = acc;
-    }
-    __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int i = tid; i < P * P; i += kThreads) {
-            a.ntpr[i] = tot[i];
-            a.rpm[i] = run[i];
-        }
-        for (int d = tid; d < P; d += kThreads) a.nrt[d] = run[(P - 1) * P + d];
-        for (int d = tid; d <= P; d += kThreads) a.part_row_base[d] = prb[d];
-    }
-    // Expert tables, spread over the grid: num_tokens_per_expert[s][e].
-    const int64_t gthreads = static_cast<int64_t>(gridDim.x) * kThreads;
-    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
-    for (int64_t i = gtid; i < static_cast<int64_t>(P) * E; i += gthreads) {
-        const int64_t s = i / E, x = i % E;
-        int32_t sum = 0;
-        for (int c = 0; c < C; ++c) sum += __ldcg(a.ecount + (s * C + c) * E + x);
-        a.ntpe[i] = sum;
-    }
-    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-    const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
-    // Channel prefixes and send_head, one warp per channel.
-    int32_t* base_all = reinterpret_cast<int32_t*>(prb + P + 1);  // [warps][P]
-    int32_t* base = base_all + warp * P;
-    const int64_t chans = static_cast<int64_t>(P) * C;
-    for (int64_t ch = gwarp; ch < chans; ch += total_warps) {
-        const int64_t s = ch / C, c = ch % C;
-        int64_t b, e;
-        split_range(a.T, C, c, &b, &e);
-        for (int d = lane; d < P; d += 32) {
-            int32_t pre = 0;
-            for (int64_t cc = 0; cc < c; ++cc) pre += __ldcg(a.ccount + (s * C + cc) * P + d);
-            const int32_t cnt = __ldcg(a.ccount + ch * P + d);
-            const int32_t rank_base = s > 0 ? run[(s - 1) * P + d] : 0;
-            a.cpm[(s * P + d) * C + c] = pre + cnt;
-            a.rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rank_base + pre;
-            base[d] = rank_base + pre;
-        }
-        __syncwarp();
-        const uint32_t below = lanemask_lt();
-        for (int64_t t0 = b; t0 < e; t0 += 32) {
-            const int64_t t = t0 + lane;
-            const bool active = t < e;
-            const int64_t g = s * a.T + t;
-            const uint8_t* row = a.itr + g * P;
-            for (int d = 0; d < P; ++d) {
-                const bool has = active && __ldcg(row + d) != 0;
-                const uint32_t bal = __ballot_sync(0xffffffffu, has);
-                const int32_t bd = base[d];
-                if (active) a.send_head[g * P + d] = has ? bd + __popc(bal & below) : -1;
-                __syncwarp();
-                if (lane == 0) base[d] = bd + __popc(bal);
-                __syncwarp();
+        const int32_t incl = warp_incl_scan(sum, lane);
+        int32_t run = carry + incl - sum;
+#pragma unroll
+        for (int u = 0; u < kSeg; ++u) {
+            const int64_t j = jb + u;
+            if (j < PC) {
+                colx[cx(j)] = run;
+                rc[j] = run;
             }
+            run += v[u];
         }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-}
-
-// ---- phase C: payload ------------------------------------------------------------
-__device__ void phase_payload(const FusedArgs& a, unsigned char* smem, const int64_t* prb_sm) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const DispatchArgs& d = a.d;
-    const uint32_t RB = static_cast<uint32_t>(a.H) * 2u;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp;
-    unsigned char* buf = smem + 128 + static_cast<size_t>(warp) * RB;
-    if (lane == 0) {
-        mbar_init(bar, 1);
-        mbar_init_fence();
-    }
+    if (lane == 0) colx[cx(PC)] = carry;
     __syncwarp();
+    for (int64_t j = lane; j < PC; j += 32) {
+        const int64_t s = static_cast<uint32_t>(j) / static_cast<uint32_t>(C), c = j - s * C;
+        a.cpm[(s * P + d) * C + c] = colx[cx(j + 1)] - colx[cx(s * C)];
+    }
+    for (int s = lane; s < P; s += 32) {
+        const int32_t hi = colx[cx(static_cast<int64_t>(s + 1) * C)], lo = colx[cx(static_cast<int64_t>(s) * C)];
+        a.ntpr[s * P + d] = hi - lo;
+        a.rpm[s * P + d] = hi;
+    }
+    if (lane == 0) a.nrt[d] = carry;
+    __syncwarp();
+}
+
+__device__ void sum_expert(const FusedArgs& a, int x, int lane) {
+    const int C = a.C, E = a.E;
+    int32_t tot = 0;
+    for (int s = lane; s < a.P; s += 32) {
+        const int32_t* src = a.ecount + static_cast<int64_t>(s) * C * E + x;
+        int32_t sum = 0;
+        for (int c0 = 0; c0 < C; c0 += kSumUnroll) {
+            int32_t v[kSumUnroll];
+#pragma unroll
+            for (int u = 0; u < kSumUnroll; ++u)
+                v[u] = c0 + u < C ? __ldcg(src + static_cast<int64_t>(c0 + u) * E) : 0;
+#pragma unroll
+            for (int u = 0; u < kSumUnroll; ++u) sum += v[u];
+        }
+        a.ntpe[static_cast<int64_t>(s) * E + x] = sum;
+        tot += sum;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) a.nrtpe[x] = static_cast<int32_t>(round_up(tot, a.A));
+}
+
+__host__ __device__ __forceinline__ int64_t colx_words(int64_t PC) { return round_up(PC + (PC >> 4) + 2, 4); }
+
+__device__ void phase_tables(const FusedArgs& a, int32_t* region) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* colx = region + warp * colx_words(a.PC);
     const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
-    // Per rank d (one warp): aligned per-expert receive counts and their
-    // offsets, summed over the source ranks of num_tokens_per_expert (phase B).
-    for (int64_t dr = static_cast<int64_t>(blockIdx.x) * kWarps + warp; dr < a.P; dr += total_warps) {
+    const int64_t tasks = static_cast<int64_t>(a.P) + a.E;
+    for (int64_t task = static_cast<int64_t>(blockIdx.x) * kWarps + warp; task < tasks; task += total_warps) {
+        if (task < a.P)
+            scan_rank_column(a, static_cast<int>(task), colx, lane);
+        else
+            sum_expert(a, static_cast<int>(task - a.P), lane);
+    }
+}
+
+// ---- phase C: payload -------------------------------------------------------------
+// Channel of source-local token t (inverse of split_range over T = cq * C + cr
+// tokens: channels below cr hold cq + 1 tokens, the others cq).
+__device__ __forceinline__ uint32_t channel_of(uint32_t t, uint32_t cq, uint32_t cr) {
+    const uint32_t big = cr * (cq + 1);
+    return t < big ? t / (cq + 1) : cr + (t - big) / cq;
+}
+
+// Per-token routing a warp needs in phase C: for destinations lane and
+// lane + 32 the local position (phase A, -1 if not sent) and the channel's
+// first row on that rank (phase B); lane k < K holds slot k's expert and weight.
+struct Route {
+    int32_t loc[2], base[2], idx;
+    float w;
+    uint32_t s, t;  // source rank and source-local token
+};
+
+__device__ __forceinline__ void load_route(const FusedArgs& a, int64_t g, int lane, Route* r) {
+    const uint32_t s = static_cast<uint32_t>(g) / static_cast<uint32_t>(a.T);
+    const uint32_t t = static_cast<uint32_t>(g) - s * static_cast<uint32_t>(a.T);
+    const int64_t ch = static_cast<int64_t>(s) * a.C + channel_of(t, a.cq, a.cr);
+    r->s = s;
+    r->t = t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int dd = lane + 32 * h;
+        r->loc[h] = dd < a.P ? __ldcg(a.send_head + g * a.P + dd) : -1;
+        r->base[h] = dd < a.P ? __ldcg(a.rcpm + dd * a.PC + ch) : 0;
+    }
+    r->idx = lane < a.K ? __ldg(a.topk_idx + g * a.K + lane) : -1;
+    r->w = (lane < a.K && a.topk_weights) ? __ldg(a.topk_weights + g * a.K + lane) : 0.f;
+}
+
+// Row buffers of one warp: token i of the warp's stream (g = first + i * step)
+// goes to buffer i % NB, completing on bars[i % NB] with parity (i / NB) & 1.
+struct Ring {
+    uint64_t* bars;
+    unsigned char* buf;
+    int64_t first, step, n_local, last_issued;
+};
+
+__device__ __forceinline__ void ring_issue(const FusedArgs& a, Ring& r, int64_t i, uint32_t RB) {
+    const int slot = static_cast<int>(i % a.nb);
+    mbar_arrive_expect_tx(&r.bars[slot], RB);
+    bulk_load(r.buf + static_cast<size_t>(slot) * RB, a.x + (r.first + i * r.step) * a.H, RB, &r.bars[slot]);
+    r.last_issued = i;
+}
+
+// After an abort: wait (bounded) for this warp's loads still in flight, so no
+// copy lands in shared memory after the CTA exits. Lane 0 only.
+__device__ void ring_drain(const FusedArgs& a, Ring& r, int64_t first) {
+    for (int64_t j = first; j <= r.last_issued; ++j)
+        mbar_wait(&r.bars[j % a.nb], static_cast<uint32_t>((j / a.nb) & 1));
+}
+
+__device__ void phase_payload(const FusedArgs& a, Ring& ring, int64_t* prb) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int P = a.P, K = a.K, NB = a.nb;
+    const DispatchArgs& d = a.d;
+    const int64_t n_local = ring.n_local;
+    const int64_t TW = static_cast<int64_t>(gridDim.x) * kWarps;
+    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    const uint32_t RB = static_cast<uint32_t>(a.H) * 2u;
+
+    Route cur, nxt;
+    if (n_local > 0) load_route(a, ring.first, lane, &cur);
+    // part_row_base: exclusive scan of num_recv_tokens (64-bit), in every CTA.
+    if (warp == 0) {
+        int64_t run = 0;
+        for (int d0 = 0; d0 < P; d0 += 32) {
+            const int dd = d0 + lane;
+            const int64_t v = dd < P ? __ldcg(a.nrt + dd) : 0;
+            int64_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (dd < P) prb[dd] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) prb[P] = run;
+        __syncwarp();
+        if (blockIdx.x == 0)
+            for (int dd = lane; dd <= P; dd += 32) a.part_row_base[dd] = prb[dd];
+    }
+    __syncthreads();
+    // recv_expert_offset: one warp per rank, exclusive scan of its experts' aligned counts.
+    for (int64_t dr = gwarp; dr < P; dr += TW) {
         int32_t carry = 0;
         for (int l0 = 0; l0 < a.epr; l0 += 32) {
             const int l = l0 + lane;
-            int64_t cnt = 0;
-            if (l < a.epr) {
-                const int64_t x = dr * a.epr + l;
-                for (int s = 0; s < a.P; ++s) cnt += __ldcg(a.ntpe + static_cast<int64_t>(s) * a.E + x);
-                cnt = round_up(cnt, a.A);
-            }
-            int32_t incl = static_cast<int32_t>(cnt);
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            if (l < a.epr) {
-                a.nrtpe[dr * a.epr + l] = static_cast<int32_t>(cnt);
-                a.reo[dr * a.epr + l] = carry + incl - static_cast<int32_t>(cnt);
-            }
+            const int32_t cnt = l < a.epr ? __ldcg(a.nrtpe + dr * a.epr + l) : 0;
+            const int32_t incl = warp_incl_scan(cnt, lane);
+            if (l < a.epr) a.reo[dr * a.epr + l] = carry + incl - cnt;
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    uint32_t phase = 0;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + warp; g < a.S; g += total_warps) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar, RB);
-            bulk_load(buf, a.x + g * a.H, RB, bar);
+
+    bool failed = false;
+    int64_t i = 0;
+    for (; i < n_local; ++i) {
+        const int slot = static_cast<int>(i % NB);
+        const int64_t g = ring.first + i * ring.step;
+        if (i + 1 < n_local) load_route(a, g + ring.step, lane, &nxt);
+        // Global send_head rows for destinations lane and lane + 32.
+        int32_t sh[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            sh[h] = cur.loc[h] >= 0 ? cur.loc[h] + cur.base[h] : -1;
+            if (cur.loc[h] >= 0) a.send_head[g * P + lane + 32 * h] = sh[h];
         }
-        const bool ok = mbar_wait(bar, phase);
-        phase ^= 1u;
+        const bool ok = mbar_wait(&ring.bars[slot], static_cast<uint32_t>((i / NB) & 1));
         if (__any_sync(0xffffffffu, !ok)) {
-            if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+            failed = true;
             break;
         }
-        for (int d0 = 0; d0 < a.P; d0 += 32) {
-            const int dd = d0 + lane;
-            const int32_t sh = dd < a.P ? __ldcg(a.send_head + g * a.P + dd) : -1;
-            if (sh >= 0) {
-                const int64_t lo = prb_sm[dd], hi = prb_sm[dd + 1], row = lo + sh;
-                if (sh < hi - lo && row >= 0 && row < d.arena_rows)
-                    bulk_store(d.arena + row * d.stride, buf, RB);
+        const unsigned char* src = ring.buf + static_cast<size_t>(slot) * RB;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int dd = lane + 32 * h;
+            if (sh[h] >= 0) {
+                const int64_t lo = prb[dd], hi = prb[dd + 1], row = lo + sh[h];
+                if (sh[h] < hi - lo && row >= 0 && row < d.arena_rows)
+                    bulk_store(d.arena + row * d.stride, src, RB);
                 else
                     raise_error(a.err, MOE_ERR_CAPACITY);
             }
         }
         bulk_commit();
-        // triple and side arrays (reads the send_head row this grid wrote)
+        // Triple and side arrays of every destination row of token g.
         {
-            const int K = a.K;
-            int32_t idx = -1;
-            float w = 0.f;
-            if (lane < K) {
-                idx = __ldg(a.topk_idx + g * K + lane);
-                if (a.topk_weights) w = __ldg(a.topk_weights + g * K + lane);
-            }
+            const int32_t idx = cur.idx;
+            const float w = cur.w;
             const int32_t dk = (idx >= 0 && idx < a.E) ? idx / a.epr : -1;
-            const int32_t src_rank = static_cast<int32_t>(g / a.T), src_tok = static_cast<int32_t>(g % a.T);
-            for (int d0 = 0; d0 < a.P; d0 += 32) {
-                const int dd = d0 + lane;
-                const int32_t sh = dd < a.P ? __ldcg(a.send_head + g * a.P + dd) : -1;
-                uint32_t todo = __ballot_sync(0xffffffffu, sh >= 0);
+            const int32_t src_rank = static_cast<int32_t>(cur.s), src_tok = static_cast<int32_t>(cur.t);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t todo = __ballot_sync(0xffffffffu, sh[h] >= 0);
                 while (todo) {
                     const int j = __ffs(todo) - 1;
                     todo &= todo - 1;
-                    const int dj = d0 + j;
-                    const int32_t shd = __shfl_sync(0xffffffffu, sh, j);
-                    const int64_t lo = prb_sm[dj], hi = prb_sm[dj + 1], row = lo + shd;
+                    const int dj = j + 32 * h;
+                    const int32_t shd = __shfl_sync(0xffffffffu, sh[h], j);
+                    const int64_t lo = prb[dj], hi = prb[dj + 1], row = lo + shd;
                     if (shd >= hi - lo || row < 0 || row >= d.arena_rows) continue;
                     const bool on = dk == dj;
                     const uint32_t kb = __ballot_sync(0xffffffffu, on);
@@ -327,48 +471,115 @@ __device__ void phase_payload(const FusedArgs& a, unsigned char* smem, const int
                 }
             }
         }
-        bulk_wait_read<0>();
+        // Refill: with two or more buffers, token i-1's buffer (its stores have
+        // left shared memory once at most one group, token i's, still reads);
+        // with one buffer, token i's own.
+        int64_t done_tok;
+        if (NB >= 2) {
+            bulk_wait_read<1>();
+            done_tok = i - 1;
+        } else {
+            bulk_wait_read<0>();
+            done_tok = i;
+        }
         __syncwarp();
+        if (lane == 0 && done_tok >= 0 && done_tok + NB < n_local) ring_issue(a, ring, done_tok + NB, RB);
+        __syncwarp();
+        cur = nxt;
     }
     bulk_wait<0>();
+    if (failed && lane == 0) {
+        raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+        ring_drain(a, ring, i);
+    }
+}
+
+// Zeroes the grid barrier counter. Launched just before fused_kernel with
+// programmatic stream serialisation: it lets fused_kernel be scheduled at once,
+// then waits for the previous work on the stream before the store; fused_kernel
+// waits for this grid to complete before it touches global memory.
+__global__ void fused_prep_kernel(unsigned int* counter) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) *counter = 0u;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_wait_then_release();
+    __shared__ int64_t prb[kMaxP + 1];
     const unsigned int n = gridDim.x;
-    phase_counts(a, smem);
-    if (!grid_barrier(a.barrier, n, a.err)) return;
-    phase_tables(a, smem);
-    if (!grid_barrier(a.barrier, 2 * n, a.err)) return;
-    // part_row_base is still in shared memory from phase B (same CTA).
-    const int64_t* prb = reinterpret_cast<const int64_t*>(reinterpret_cast<int32_t*>(smem) + 2 * a.P * a.P);
-    // Copy it out of the area phase C reuses for its buffers.
-    __shared__ int64_t prb_sm[kMaxP + 1];
-    for (int i = threadIdx.x; i <= a.P; i += blockDim.x) prb_sm[i] = prb[i];
-    // The shared memory written by phases A and B is reused by bulk copies.
-    fence_proxy_async_smem();
-    __syncthreads();
-    phase_payload(a, smem, prb_sm);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t RB = static_cast<uint32_t>(a.H) * 2u;
+    int32_t* region = reinterpret_cast<int32_t*>(smem + a.ab_off);
+
+    // Start the row loads of each warp's first tokens: they overlap phases A and B.
+    Ring ring;
+    ring.bars = reinterpret_cast<uint64_t*>(smem) + warp * kMaxNB;
+    ring.buf = smem + kBarBytes + static_cast<size_t>(warp) * a.nb * RB;
+    // Tokens are dealt to CTAs first (g mod gridDim), so every SM -- whose
+    // bulk-copy engine all its warps share -- gets the same number of rows.
+    ring.first = blockIdx.x + static_cast<int64_t>(n) * warp;
+    ring.step = static_cast<int64_t>(n) * kWarps;
+    ring.n_local = ring.first < a.S ? (a.S - 1 - ring.first) / ring.step + 1 : 0;
+    ring.last_issued = -1;
+    if (lane == 0) {
+        for (int b = 0; b < a.nb; ++b) mbar_init(&ring.bars[b], 1);
+        mbar_init_fence();
+        const int64_t npro = ring.n_local < a.nb ? ring.n_local : a.nb;
+        for (int64_t i = 0; i < npro; ++i) ring_issue(a, ring, i, RB);
+    }
+    __syncwarp();
+
+    // err starts at 0: CTA 0 clears it before the first grid barrier, and every
+    // status is raised after that barrier.
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.err) *a.err = 0;
+    const bool bad = __syncthreads_or(phase_counts(a, region));
+    bool ok = grid_barrier(a.barrier, n, a.err);
+    if (ok) {
+        if (bad && threadIdx.x == 0) raise_error(a.err, MOE_ERR_TOPK_OUT_OF_RANGE);
+        phase_tables(a, region);
+        ok = grid_barrier(a.barrier, 2 * n, a.err);
+    }
+    if (!ok) {
+        if (lane == 0) ring_drain(a, ring, 0);
+        return;
+    }
+    phase_payload(a, ring, prb);
 }
 
-size_t fused_smem(const moe_shape& s) {
-    const size_t a = static_cast<size_t>(kWarps) * (s.E + s.P) * 4;
-    const size_t b = static_cast<size_t>(2 * s.P * s.P) * 4 + static_cast<size_t>(s.P + 1) * 8 +
-                     static_cast<size_t>(kWarps) * s.P * 4;
-    const size_t c = 128 + static_cast<size_t>(kWarps) * s.H * 2;
-    size_t m = a > b ? a : b;
-    return m > c ? m : c;
+// Row buffers per warp, the offset of the phase A / B region and the dynamic
+// shared memory of the launch, for a budget of `limit` bytes.
+void fused_plan(const moe_shape& s, int64_t limit, int* nb, uint32_t* ab_off, size_t* smem) {
+    const int64_t pc = static_cast<int64_t>(s.P) * s.num_channels;
+    const int64_t a = static_cast<int64_t>(kWarps) * s.E * 4;
+    const int64_t b = static_cast<int64_t>(kWarps) * colx_words(pc) * 4;
+    const int64_t ab = a > b ? a : b;
+    const int64_t rb = static_cast<int64_t>(s.H) * 2;
+    const int64_t avail = limit - kBarBytes - ab;
+    int64_t n = avail > 0 ? avail / (kWarps * rb) : 0;
+    n = n > kMaxNB ? kMaxNB : n;
+    *nb = static_cast<int>(n);
+    *ab_off = static_cast<uint32_t>(kBarBytes + kWarps * n * rb);
+    *smem = static_cast<size_t>(*ab_off + ab);
 }
 
 }  // namespace
 
 bool fused_supported(const moe_shape& s) {
-    return s.P <= kMaxP && s.E <= kMaxE && s.H <= kMaxH && s.quant == 0;
+    if (!(s.P <= kMaxP && s.E <= kMaxE && s.H <= kMaxH && s.K <= kMaxK && s.quant == 0 &&
+          static_cast<int64_t>(s.P) * s.num_channels <= kMaxPC))
+        return false;
+    int nb = 0;
+    uint32_t off = 0;
+    size_t smem = 0;
+    fused_plan(s, kSmemBudget, &nb, &off, &smem);
+    return nb >= 1;
 }
 
 int64_t fused_scratch_bytes(const moe_shape& s) {
-    const int64_t chans = static_cast<int64_t>(s.P) * s.num_channels;
-    return round_up(chans * (s.P + s.E) * 4 + 256, 256);
+    const int64_t pc = static_cast<int64_t>(s.P) * s.num_channels;
+    return round_up(256 + (static_cast<int64_t>(s.P) * round_up(pc, 4) + pc * s.E) * 4, 256);
 }
 
 cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* topk_idx, const float* topk_weights,
@@ -386,6 +597,10 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     a.epr = s.E / s.P;
     a.S = s.S;
     a.T = s.S / s.P;
+    a.PC = static_cast<int64_t>(s.P) * s.num_channels;
+    a.PCp = round_up(a.PC, 4);
+    a.cq = static_cast<uint32_t>(a.T / s.num_channels);
+    a.cr = static_cast<uint32_t>(a.T % s.num_channels);
     a.x = x;
     a.topk_idx = topk_idx;
     a.topk_weights = topk_weights;
@@ -402,30 +617,51 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     a.send_head = send_head;
     a.part_row_base = part_row_base;
     a.d = d;
-    const int64_t chans = static_cast<int64_t>(s.P) * s.num_channels;
     unsigned char* sc = static_cast<unsigned char*>(scratch);
     a.barrier = reinterpret_cast<unsigned int*>(sc);
-    a.ccount = reinterpret_cast<int32_t*>(sc + 256);
-    a.ecount = a.ccount + chans * s.P;
+    a.ccT = reinterpret_cast<int32_t*>(sc + 256);
+    a.ecount = a.ccT + a.PCp * s.P;
     a.err = err;
-    const size_t smem = fused_smem(s);
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, fused_kernel);
+    if (e != cudaSuccess) return e;
+    int64_t limit = static_cast<int64_t>(optin) - static_cast<int64_t>(fa.sharedSizeBytes);
+    if (limit > kSmemBudget) limit = kSmemBudget;
+    size_t smem = 0;
+    fused_plan(s, limit, &a.nb, &a.ab_off, &smem);
+    if (a.nb < 1) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = device_sm_count();  // one CTA per SM: all resident (cooperative launch)
-    e = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned int), stream);
+    e = launch_pdl(fused_prep_kernel, 1, 32, 0, stream, a.barrier);
     if (e != cudaSuccess) return e;
-    if (err) {
-        e = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
-        if (e != cudaSuccess) return e;
-    }
-    void* args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_kernel), dim3(grid), dim3(kThreads),
-                                       args, smem, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, fused_kernel, a);
+    if (e == cudaSuccess) return e;
+    // Without programmatic serialisation the launch simply follows the prep kernel.
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_kernel, a);
 }
 
 }  // namespace moe

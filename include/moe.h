@@ -234,11 +234,13 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
  * (part_row_base is written here and used for the rows).
  *
  * One cooperative persistent kernel (one CTA per SM) with two bounded grid
- * barriers; the barrier counter lives in scratch and is zeroed on the stream
- * before the launch, as is `err` (then raised to MOE_ERR_TOPK_OUT_OF_RANGE,
- * MOE_ERR_CAPACITY or MOE_ERR_DEVICE_TIMEOUT if needed).
- * Supported: P <= 64, E <= 1024, H <= 8192, quant = 0; other shapes return
- * MOE_ERR_UNSUPPORTED (use the separate calls). scratch >= moe_scratch_bytes.
+ * barriers; the barrier counter lives in scratch and is zeroed by a one-thread
+ * kernel launched on the stream just before. `err` is always written: cleared by the kernel, then
+ * raised to MOE_ERR_TOPK_OUT_OF_RANGE, MOE_ERR_CAPACITY or
+ * MOE_ERR_DEVICE_TIMEOUT if needed.
+ * Supported: P <= 64, E <= 1024, H <= 8192, K <= 16, P * num_channels <= 4096,
+ * quant = 0; other shapes return MOE_ERR_UNSUPPORTED (use the separate calls).
+ * scratch >= moe_scratch_bytes.
  */
 moe_status moe_dispatch_fused(const moe_shape* shape, const uint16_t* x, const int32_t* topk_idx,
                               const float* topk_weights, int32_t* num_tokens_per_rank,
