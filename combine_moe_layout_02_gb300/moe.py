@@ -26,7 +26,11 @@ MOE_ERR_INCONSISTENT = 7
 EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scratch_bytes",
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
            "moe_layout_static_scratch", "moe_pad_partitions", "moe_max_expert_rows",
-           "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused")
+           "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused",
+           "moe_run_host_workspace_bytes", "moe_run_host")
+
+# moe_run_host flag (include/moe.h).
+MOE_RUN_FUSED = 1
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
 MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -101,6 +105,10 @@ def lib() -> ctypes.CDLL:
     L.moe_pad_partitions.argtypes = [sp, vp, vp, vp, i64, vp, vp, vp, vp]
     L.moe_layout_static_scratch.restype = i32
     L.moe_layout_static_scratch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_run_host_workspace_bytes.restype = i64
+    L.moe_run_host_workspace_bytes.argtypes = [sp, i32]
+    L.moe_run_host.restype = i32
+    L.moe_run_host.argtypes = [sp, i32, vp, vp, vp, vp, vp, i64, i32, vp, i64, vp]
     _lib = L
     return L
 
@@ -257,6 +265,57 @@ def moe_layout_static_scratch(shape, topk_idx, num_tokens_per_rank, num_tokens_p
                                          _ptr(num_tokens_per_expert), _ptr(is_token_in_rank),
                                          _ptr(is_token_in_rank_bits), _ptr(err), _stream(stream))
     _check(st, "moe_layout_static_scratch")
+
+
+def _host_ptr(t):
+    """Host address of a contiguous CPU tensor or numpy array (None -> NULL)."""
+    if t is None:
+        return None
+    if hasattr(t, "is_cuda"):
+        if t.is_cuda:
+            raise ValueError("expected a host tensor")
+        if not t.is_contiguous():
+            raise ValueError("expected a contiguous tensor")
+        return t.data_ptr()
+    if not t.flags["C_CONTIGUOUS"]:
+        raise ValueError("expected a contiguous array")
+    return t.ctypes.data
+
+
+def moe_run_host_workspace_bytes(shape: moe_shape, n_batches: int) -> int:
+    return int(lib().moe_run_host_workspace_bytes(ctypes.byref(shape), int(n_batches)))
+
+
+def moe_run_host(shape: moe_shape, x_host, topk_idx_host, topk_weights_host, out_host, workspace,
+                 y=None, y_row_stride=0, fused=False, err_host=None):
+    """Run the path over len(x_host) host-resident batches end to end.
+
+    x_host / topk_idx_host / out_host: sequences of host tensors (pinned for
+    overlap), one per batch; topk_weights_host: such a sequence or None.
+    workspace: device uint8 tensor of moe_run_host_workspace_bytes bytes.
+    err_host: None or an int32 numpy array of n batches (device error words).
+    Blocking; raises MoeError on any non-OK status.
+    """
+    n = len(x_host)
+    if len(topk_idx_host) != n or len(out_host) != n or (topk_weights_host is not None
+                                                         and len(topk_weights_host) != n):
+        raise ValueError("one entry per batch in every host list")
+    arr = ctypes.c_void_p * max(n, 1)
+    xs = arr(*[_host_ptr(t) for t in x_host])
+    ids = arr(*[_host_ptr(t) for t in topk_idx_host])
+    ws = arr(*[_host_ptr(t) for t in topk_weights_host]) if topk_weights_host is not None else None
+    outs = arr(*[_host_ptr(t) for t in out_host])
+    eh = None
+    if err_host is not None:
+        if err_host.dtype.itemsize != 4 or err_host.size < n:
+            raise ValueError("err_host: int32 array of one entry per batch")
+        eh = err_host.ctypes.data
+    st = lib().moe_run_host(ctypes.byref(shape), n, ctypes.cast(xs, ctypes.c_void_p),
+                            ctypes.cast(ids, ctypes.c_void_p),
+                            ctypes.cast(ws, ctypes.c_void_p) if ws is not None else None,
+                            ctypes.cast(outs, ctypes.c_void_p), _ptr(y), int(y_row_stride),
+                            MOE_RUN_FUSED if fused else 0, _ptr(workspace), workspace.numel(), eh)
+    _check(st, "moe_run_host")
 
 
 class Buffers:

@@ -349,6 +349,51 @@ moe_status moe_layout_static_scratch(const moe_shape* shape, const int32_t* topk
                                      uint8_t* is_token_in_rank, uint32_t* is_token_in_rank_bits,
                                      int32_t* err, void* stream);
 
+/*
+ * moe_run_host -- the whole path (moe_layout -> moe_notify -> moe_dispatch ->
+ * moe_combine, or moe_dispatch_fused -> moe_combine) over n_batches batches
+ * held in HOST memory, end to end: each batch's x, topk_idx and topk_weights
+ * are copied to the device, routed, exchanged and reduced, and its combined
+ * rows are copied back to out_host[i]. The pages have no single call for
+ * this; it is the serving loop around the path ("Ascend DeepEP MoE Dispatch
+ * Optimization", section "一条 token 如何走完 MoE": route, exchange, reduce,
+ * per batch).
+ *
+ * Three internal streams overlap consecutive batches: while batch i computes,
+ * batch i + 1's inputs are copied in and batch i - 1's output is copied out.
+ * Inputs and outputs are double-buffered in the workspace; all other buffers
+ * are used in batch order. The call is blocking: it first waits for all work
+ * already submitted to the device, and returns when every copy has landed in
+ * host memory. It is not capturable in a CUDA graph.
+ *
+ *   x_host[i]            bf16 bits [S,H] of batch i (pinned host memory for
+ *                        copies that overlap; any host memory is accepted)
+ *   topk_idx_host[i]     int32 [S,K]
+ *   topk_weights_host    NULL (unit weights, as in moe_combine) or an array of
+ *                        n_batches pointers to float [S,K]
+ *   out_host[i]          bf16 bits [S,H], written with batch i's combine
+ *                        result; entries may alias (batches are written back
+ *                        in order)
+ *   y, y_row_stride      expert outputs read by combine, device memory of at
+ *                        least moe_max_recv_rows(shape) rows; NULL means
+ *                        identity experts (combine reads the bf16 dispatch
+ *                        arena, quant must be 0)
+ *   flags                0, or MOE_RUN_FUSED: use moe_dispatch_fused when it
+ *                        supports the shape (otherwise the separate calls)
+ *   workspace            >= moe_run_host_workspace_bytes(shape, n_batches)
+ *                        device bytes, 256-byte aligned, owned by the caller
+ *   err_host             NULL or int32 [n_batches] host array: each batch's
+ *                        device error word (0, or a moe_status code)
+ * Returns MOE_OK, a host-side error (nothing run), MOE_ERR_CUDA, or the first
+ * nonzero device error word in batch order.
+ */
+#define MOE_RUN_FUSED 1
+int64_t moe_run_host_workspace_bytes(const moe_shape* shape, int32_t n_batches);
+moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_t* const* x_host,
+                        const int32_t* const* topk_idx_host, const float* const* topk_weights_host,
+                        uint16_t* const* out_host, const void* y, int64_t y_row_stride, int32_t flags,
+                        void* workspace, int64_t workspace_bytes, int32_t* err_host);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -77,3 +77,34 @@ def test_static_scratch_size_guard_runs_on_the_host(lib):
                                          None) == moe.MOE_ERR_UNSUPPORTED
     assert lib.moe_layout_static_scratch(big, None, fake, fake, fake, None, None,
                                          None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_run_host_checks_arguments_on_the_host(lib):
+    """moe_run_host validates everything before it touches a device (the fake
+    device pointers below are never dereferenced)."""
+    import ctypes
+
+    s = moe.make_shape(4, 16, 64, 2, 64)
+    n = 2
+    arr = (ctypes.c_void_p * n)(*([1 << 20] * n))
+    need = moe.moe_run_host_workspace_bytes(s, n)
+    assert need > 0 and moe.moe_run_host_workspace_bytes(s, -1) == -1
+    ws = 1 << 24
+    args = lambda **k: dict(dict(x=arr, i=arr, w=None, o=arr, y=None, ys=0, fl=0, wsp=ws, wsb=need), **k)
+
+    def call(shape=s, nb=n, **k):
+        a = args(**k)
+        return lib.moe_run_host(shape, nb, a["x"], a["i"], a["w"], a["o"], a["y"], a["ys"], a["fl"],
+                                a["wsp"], a["wsb"], None)
+
+    assert call(nb=0) == moe.MOE_OK                       # nothing to run
+    assert call(nb=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(fl=2) == moe.MOE_ERR_INVALID_ARG          # unknown flag
+    assert call(wsb=need - 1) == moe.MOE_ERR_INVALID_ARG  # workspace too small
+    assert call(wsp=ws + 16) == moe.MOE_ERR_INVALID_ARG   # workspace not 256-byte aligned
+    assert call(x=None) == moe.MOE_ERR_INVALID_ARG
+    q = moe.make_shape(4, 16, 64, 2, 64, quant=1)
+    need_q = moe.moe_run_host_workspace_bytes(q, n)
+    assert call(shape=q, wsb=need_q) == moe.MOE_ERR_INVALID_ARG  # int8 slots need expert outputs y
+    holes = (ctypes.c_void_p * n)(1 << 20, None)
+    assert call(o=holes) == moe.MOE_ERR_INVALID_ARG      # a batch without an output buffer
