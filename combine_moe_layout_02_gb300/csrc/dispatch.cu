@@ -80,25 +80,38 @@ __host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_
     // full[kMaxStages] then empty[kMaxStages] (the bf16 kernel uses full only)
     l.ring = l.bars + static_cast<size_t>(round_up(2 * kMaxStages * 8, 128));
     l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
-    l.total = l.qbuf + (quant ? kInt8Consumers * static_cast<size_t>(round_up(H, 128)) : 0);
+    // two int8 rows per consumer: one is quantised while the other's stores drain
+    l.total = l.qbuf + (quant ? 2 * kInt8Consumers * static_cast<size_t>(round_up(H, 128)) : 0);
     return l;
 }
 
+// Routing words of token g a warp needs for its copies and metadata: lane k < K
+// holds slot k's expert and weight, lane d < 32 send_head[g][d].
+struct TokenRoute {
+    int32_t idx, sh0;
+    float w;
+};
+
+__device__ __forceinline__ TokenRoute load_token_route(const DispatchArgs& a, int64_t g, int lane) {
+    TokenRoute r;
+    r.idx = lane < a.K ? __ldg(a.topk_idx + g * a.K + lane) : -1;
+    r.w = (lane < a.K && a.topk_weights) ? __ldg(a.topk_weights + g * a.K + lane) : 0.f;
+    r.sh0 = lane < a.P ? __ldg(a.send_head + g * a.P + lane) : -1;
+    return r;
+}
+
 // Triple + side arrays for every destination of token g; one warp.
-__device__ void write_token_meta(const DispatchArgs& a, const int64_t* prb, int64_t g, int lane) {
+__device__ __forceinline__ void write_token_meta(const DispatchArgs& a, const int64_t* prb, int64_t g, int lane,
+                                 TokenRoute rt) {
     const int K = a.K;
-    int32_t idx = -1;
-    float w = 0.f;
-    if (lane < K) {
-        idx = __ldg(a.topk_idx + g * K + lane);
-        if (a.topk_weights) w = __ldg(a.topk_weights + g * K + lane);
-    }
+    const int32_t idx = rt.idx;
+    const float w = rt.w;
     const int32_t dk = (idx >= 0 && idx < a.E) ? idx / a.epr : -1;
     const int32_t src_rank = static_cast<int32_t>(g / a.T);
     const int32_t src_tok = static_cast<int32_t>(g % a.T);
     for (int d0 = 0; d0 < a.P; d0 += 32) {
         const int d = d0 + lane;
-        const int32_t sh = d < a.P ? __ldg(a.send_head + g * a.P + d) : -1;
+        const int32_t sh = d0 == 0 ? rt.sh0 : (d < a.P ? __ldg(a.send_head + g * a.P + d) : -1);
         uint32_t todo = __ballot_sync(0xffffffffu, sh >= 0);
         while (todo) {
             const int j = __ffs(todo) - 1;
@@ -200,10 +213,12 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
 
     if (warp != 0) {
         for (int64_t i = warp - 1; i < n_local; i += nwarps - 1) {
-            if constexpr (EXPERT)
+            if constexpr (EXPERT) {
                 write_slot_meta(a, prb, blockIdx.x + i * G, lane);
-            else
-                write_token_meta(a, prb, blockIdx.x + i * G, lane);
+            } else {
+                const int64_t g = blockIdx.x + i * G;
+                write_token_meta(a, prb, g, lane, load_token_route(a, g, lane));
+            }
         }
         return;
     }
@@ -289,6 +304,28 @@ __device__ __forceinline__ int32_t quant_one(float x, float scale, float r, bool
     int32_t q = __float2int_rn(t);
     if (!(fast && fabsf(t - __int2float_rn(q)) < 0.5f - 0x1p-15f)) q = __float2int_rn(__fdiv_rn(x, scale));
     return q;
+}
+
+// Adding 1.5 * 2^23 to a binary32 |t| < 2^22 rounds it to an integer, half to
+// even (IEEE round to nearest); the sum's low byte is then that integer mod 256.
+constexpr float kRoundMagic = 12582912.0f;
+
+// 4 bf16 (two words) -> 4 int8 bytes of rint(x * r), with no conversion
+// instructions. `near` is set when some t = x * r lies within 2^-15 of a
+// half-integer, where rounding t may differ from rounding x / scale (see
+// quant_one); the caller then redoes the chunk with division.
+__device__ __forceinline__ uint32_t quant_fast4(uint32_t w0, uint32_t w1, float r, bool& near) {
+    const float x[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+    uint32_t b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float t = __fmul_rn(x[i], r);
+        const float u = __fadd_rn(t, kRoundMagic);
+        const float d = __fsub_rn(t, __fsub_rn(u, kRoundMagic));
+        near |= fabsf(d) >= 0.5f - 0x1p-15f;
+        b[i] = __float_as_uint(u);
+    }
+    return __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
 }
 
 // 8 bf16 (one 16-byte chunk) -> 8 int8, packed little-endian.
@@ -380,11 +417,15 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     }
 
     const int cw = warp - 1;
-    unsigned char* q = smem + L.qbuf + static_cast<size_t>(cw) * qstride;
+    unsigned char* qbase = smem + L.qbuf + static_cast<size_t>(cw) * 2 * qstride;
     const int nchunks = a.H / 8;
-    for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
+    int qi = 0;
+    for (int64_t i = cw; i < n_local; i += kInt8Consumers, qi ^= 1) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
+        // Routing words load while the row arrives and is quantised.
+        TokenRoute rt;
+        if constexpr (!EXPERT) rt = load_token_route(a, g, lane);
         const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>((i / NS) & 1));
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
@@ -399,11 +440,24 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         const bool zero = m == 0.f;
         const float r = zero ? 0.f : __frcp_rn(scale);
         const bool fast = !zero && isfinite(r);
-        // This warp's previous stores must have finished reading q.
-        bulk_wait_read<0>();
+        // The stores of this warp's token before last read the same int8 row;
+        // at most one group (the last token's, other row) may still read.
+        unsigned char* q = qbase + static_cast<size_t>(qi) * qstride;
+        bulk_wait_read<1>();
         __syncwarp();
-        for (int j = lane; j < nchunks; j += 32)
-            reinterpret_cast<uint2*>(q)[j] = quant_chunk(row[j], scale, r, fast, zero);
+        for (int j = lane; j < nchunks; j += 32) {
+            const uint4 v = row[j];
+            uint2 o;
+            if (fast) {
+                bool near = false;
+                o.x = quant_fast4(v.x, v.y, r, near);
+                o.y = quant_fast4(v.z, v.w, r, near);
+                if (near) o = quant_chunk(v, scale, r, false, false);
+            } else {
+                o = quant_chunk(v, scale, r, false, zero);
+            }
+            reinterpret_cast<uint2*>(q)[j] = o;
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);  // ring slot read by every lane
@@ -414,7 +468,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                 int64_t rowi;
                 dst = expert_slot_of(a, prb, g, d, &rowi);
             } else {
-                const int32_t sh = __ldg(a.send_head + g * a.P + d);
+                const int32_t sh = d < 32 ? rt.sh0 : __ldg(a.send_head + g * a.P + d);
                 if (sh >= 0) dst = slot_of(a, prb, d, sh);
             }
             if (dst) {
@@ -429,7 +483,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         if constexpr (EXPERT)
             write_slot_meta(a, prb, g, lane);
         else
-            write_token_meta(a, prb, g, lane);
+            write_token_meta(a, prb, g, lane, rt);
     }
     bulk_wait<0>();
 }
