@@ -24,9 +24,11 @@
 //  * int8: a producer warp streams rows into the ring (full / empty
 //    mbarriers); consumer warps each take whole tokens: amax by a warp
 //    reduction, quantisation (exact round-half-even of x / scale, see
-//    quant_one) into the warp's own shared int8 row, then the same bulk stores
-//    fan that row out. A small ring and few consumers per CTA, so several CTAs
-//    (and producers) share an SM.
+//    quant_one and quant_fast4) written in place over the front of the bf16
+//    row in its ring slot, then the same bulk stores fan that row out. The
+//    slot goes back to the producer once those stores have read it. Small
+//    rings (one slot per consumer) and few consumers per CTA, so many CTAs
+//    -- and so many quantising warps -- share an SM.
 // Every mbarrier wait is bounded; on time-out the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains its own copies (bounded) and returns.
 #include <cuda_bf16.h>
@@ -69,7 +71,7 @@ static_assert(kStoreDepth >= 1 && kStoreDepth < kMaxStages, "store depth must le
 static_assert(kMaxStages >= kInt8Consumers, "the int8 ring needs a slot per consumer warp");
 
 struct DispatchSmem {
-    size_t prb, bars, ring, qbuf, total;
+    size_t prb, bars, ring, total;
 };
 
 __host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes, int H,
@@ -79,9 +81,8 @@ __host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_
     l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
     // full[kMaxStages] then empty[kMaxStages] (the bf16 kernel uses full only)
     l.ring = l.bars + static_cast<size_t>(round_up(2 * kMaxStages * 8, 128));
-    l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
-    // two int8 rows per consumer: one is quantised while the other's stores drain
-    l.total = l.qbuf + (quant ? 2 * kInt8Consumers * static_cast<size_t>(round_up(H, 128)) : 0);
+    // int8 rows are written in place over their bf16 source in the ring
+    l.total = l.ring + static_cast<size_t>(stages) * row_bytes;
     return l;
 }
 
@@ -371,14 +372,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // barrier on the token path.
 template <bool EXPERT>
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
-    pdl_wait_then_release();
+    // Waits for the previous kernel but does not let the next one be scheduled
+    // early: with many small CTAs per SM here, the next kernel's CTAs resident
+    // beside these slowed the pair down (measured: dispatch + combine 835 vs
+    // 761 us at P=8, H=7168). The next kernel launches as these CTAs exit.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(128) unsigned char smem[];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, true);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kMaxStages;
     unsigned char* ring = smem + L.ring;
-    const size_t qstride = static_cast<size_t>(round_up(a.H, 128));
     for (int i = threadIdx.x; i <= a.P; i += blockDim.x) prb[i] = a.part_row_base[i];
     if (threadIdx.x == 0) {
         for (int st = 0; st < a.stages; ++st) {
@@ -417,10 +421,10 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     }
 
     const int cw = warp - 1;
-    unsigned char* qbase = smem + L.qbuf + static_cast<size_t>(cw) * 2 * qstride;
     const int nchunks = a.H / 8;
-    int qi = 0;
-    for (int64_t i = cw; i < n_local; i += kInt8Consumers, qi ^= 1) {
+    const int spc = NS / kInt8Consumers;  // ring slots per consumer
+    int64_t last_i = -1;
+    for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
         // Routing words load while the row arrives and is quantised.
@@ -440,27 +444,30 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         const bool zero = m == 0.f;
         const float r = zero ? 0.f : __frcp_rn(scale);
         const bool fast = !zero && isfinite(r);
-        // The stores of this warp's token before last read the same int8 row;
-        // at most one group (the last token's, other row) may still read.
-        unsigned char* q = qbase + static_cast<size_t>(qi) * qstride;
-        bulk_wait_read<1>();
-        __syncwarp();
-        for (int j = lane; j < nchunks; j += 32) {
-            const uint4 v = row[j];
-            uint2 o;
-            if (fast) {
-                bool near = false;
-                o.x = quant_fast4(v.x, v.y, r, near);
-                o.y = quant_fast4(v.z, v.w, r, near);
-                if (near) o = quant_chunk(v, scale, r, false, false);
-            } else {
-                o = quant_chunk(v, scale, r, false, zero);
+        // In place: the int8 row overwrites the front of the ring slot. Chunk j's
+        // 8 bytes land in bf16 chunks j/2, already read (syncwarp between the
+        // reads and writes of one iteration).
+        unsigned char* q = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(row));
+        for (int j0 = 0; j0 < nchunks; j0 += 32) {
+            const int j = j0 + lane;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (j < nchunks) v = row[j];
+            uint2 o = make_uint2(0, 0);
+            if (j < nchunks) {
+                if (fast) {
+                    bool near = false;
+                    o.x = quant_fast4(v.x, v.y, r, near);
+                    o.y = quant_fast4(v.z, v.w, r, near);
+                    if (near) o = quant_chunk(v, scale, r, false, false);
+                } else {
+                    o = quant_chunk(v, scale, r, false, zero);
+                }
             }
-            reinterpret_cast<uint2*>(q)[j] = o;
+            __syncwarp();
+            if (j < nchunks) reinterpret_cast<uint2*>(q)[j] = o;
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);  // ring slot read by every lane
         const int nfan = EXPERT ? a.K : a.P;
         for (int d = lane; d < nfan; d += 32) {
             uint8_t* dst = nullptr;
@@ -484,6 +491,22 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
             write_slot_meta(a, prb, g, lane);
         else
             write_token_meta(a, prb, g, lane, rt);
+        if (spc >= 2) {
+            // token i - kInt8Consumers (this warp's previous) has left its slot
+            bulk_wait_read<1>();
+            __syncwarp();
+            if (lane == 0 && i >= kInt8Consumers) mbar_arrive(&empty[(i - kInt8Consumers) % NS]);
+        } else {
+            bulk_wait_read<0>();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        last_i = i;
+    }
+    if (spc >= 2 && last_i >= 0) {
+        bulk_wait_read<0>();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[last_i % NS]);
     }
     bulk_wait<0>();
 }
