@@ -110,3 +110,11 @@ def test_device_errors_are_reported_per_batch():
     assert err.tolist() == [0, moe.MOE_ERR_TOPK_OUT_OF_RANGE, 0]
     # Batches without the bad id are still exact (pageable host buffers work too).
     np.testing.assert_array_equal(outs[2].numpy().view(np.uint16), _expected(ws[2], weights=False))
+
+
+def test_fused_flag_falls_back_where_the_fused_kernel_does_not_apply():
+    # P = 80 is beyond the fused kernel's limit: the separate calls run instead.
+    ws = _batches(80, 160, 3, 64, 2, 2)
+    got = _run(ws, fused=True)
+    for w, g in zip(ws, got):
+        np.testing.assert_array_equal(g, _expected(w))
