@@ -306,33 +306,34 @@ def run_ours(args, world, rank, local):
 
     fused = args.fused
 
-    def step(ev=None):
+    def step(ev=None, st=None):
+        st = stream if st is None else st
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         if fused:
             # layout + notify + dispatch in one launch: timed as "dispatch"
             if ev is not None:
-                ev[1].record(stream)
-            buf.dispatch_fused(x, idx, wts, stream)
+                ev[1].record(st)
+            buf.dispatch_fused(x, idx, wts, st)
         else:
-            buf.layout(idx, stream)
-            buf.notify(stream)
+            buf.layout(idx, st)
+            buf.notify(st)
             if expert:
-                buf.notify_expert(idx, stream)
+                buf.notify_expert(idx, st)
             if ev is not None:
-                ev[1].record(stream)
+                ev[1].record(st)
             if expert:
-                buf.dispatch_expert(x, idx, wts, stream)
+                buf.dispatch_expert(x, idx, wts, st)
             else:
-                buf.dispatch(x, idx, wts, stream)
+                buf.dispatch(x, idx, wts, st)
         if ev is not None:
-            ev[2].record(stream)
+            ev[2].record(st)
         if expert:
-            buf.combine_expert(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=stream)
+            buf.combine_expert(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=st)
         else:
-            buf.combine(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=stream)
+            buf.combine(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=st)
         if ev is not None:
-            ev[3].record(stream)
+            ev[3].record(st)
 
     for _ in range(args.warmup):
         step()
@@ -377,10 +378,25 @@ def run_ours(args, world, rank, local):
             uuid = "GPU-" + uuid
     except Exception:
         uuid = None
+    timed_step = step
+    if args.graph:
+        # One step captured as a CUDA graph, replayed in the timed region: the
+        # launches of a small step cost more host time than its kernels.
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            step(st=torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        if int(buf.err[0].item()) != 0:
+            raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")
+        timed_step = graph.replay
     with ClockSampler(uuid) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        elapsed_s = run_steps(args.steps, step)
+        elapsed_s = run_steps(args.steps, timed_step)
         barrier(world)
     clk = clocks.summary()
     max_s, units = aggregate(elapsed_s, float(w.S * args.steps), world)
@@ -463,7 +479,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
-                       fused=bool(args.fused),
+                       fused=bool(args.fused), graph=bool(args.graph),
                        l2=("no flush: working set (x, receive arena, out) of "
                            f"{footprint / 1e6:.0f} MB is larger than twice the {l2 / 1e6:.0f} MB L2"
                            if flush_buf is None else
@@ -503,6 +519,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
                     help="receive layout: one row per (token, rank), or one per (token, k) grouped by expert")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step as a CUDA graph and replay it in the timed region")
     ap.add_argument("--fused", action="store_true",
                     help="layout + notify + dispatch as one cooperative launch (small shapes)")
     ap.add_argument("--tokens-per-rank", type=int, default=None,

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe.h"
 #include "moe_device.cuh"
 
@@ -18,6 +20,83 @@ int device_sm_count() {
     if (n < 1) n = 1;
     if (dev >= 0 && dev < 64) cached[dev] = n;
     return n;
+}
+
+int device_optin_smem() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 48 * 1024;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 48 * 1024;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+namespace {
+
+// Per (kernel, device): the dynamic shared memory the kernel has been allowed
+// so far, its static shared memory, and the last occupancy query. Launches
+// then skip repeated runtime queries; the allowance only ever grows, so a
+// concurrent launch with a smaller request stays valid.
+struct KernelEntry {
+    const void* fn;
+    int dev, smem_allowed, occ_threads, occ, static_smem;
+    size_t occ_smem;
+};
+std::mutex g_kernel_mu;
+KernelEntry g_kernels[256];
+int g_nkernels = 0;
+
+KernelEntry* kernel_entry(const void* fn, int dev) {  // g_kernel_mu held
+    for (int i = 0; i < g_nkernels; ++i)
+        if (g_kernels[i].fn == fn && g_kernels[i].dev == dev) return &g_kernels[i];
+    if (g_nkernels == 256) return nullptr;
+    g_kernels[g_nkernels] = KernelEntry{fn, dev, 0, -1, 0, -1, 0};
+    return &g_kernels[g_nkernels++];
+}
+
+}  // namespace
+
+cudaError_t prepare_kernel(const void* fn, size_t smem, int threads, int* per_sm) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_kernel_mu);
+    KernelEntry* k = kernel_entry(fn, dev);
+    if (k == nullptr || static_cast<int64_t>(smem) > k->smem_allowed) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (k) k->smem_allowed = static_cast<int>(smem);
+    }
+    if (per_sm) {
+        if (k == nullptr || k->occ_threads != threads || k->occ_smem != smem) {
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+            if (e != cudaSuccess) return e;
+            if (k) {
+                k->occ_threads = threads;
+                k->occ_smem = smem;
+                k->occ = n;
+            }
+            *per_sm = n;
+        } else {
+            *per_sm = k->occ;
+        }
+    }
+    return cudaSuccess;
+}
+
+int kernel_static_smem(const void* fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(g_kernel_mu);
+    KernelEntry* k = kernel_entry(fn, dev);
+    if (k && k->static_smem >= 0) return k->static_smem;
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return -1;
+    if (k) k->static_smem = static_cast<int>(fa.sharedSizeBytes);
+    return static_cast<int>(fa.sharedSizeBytes);
 }
 
 namespace {

@@ -196,8 +196,8 @@ template <int MAXR, bool EXPERT>
 cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(a.P + 1) * 8;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<MAXR, EXPERT>,
-                                                                  kCombineThreads, smem);
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(combine_kernel<MAXR, EXPERT>), smem,
+                                   kCombineThreads, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t warps_per_block = kCombineThreads / 32;

@@ -533,18 +533,12 @@ cudaError_t launch_dispatch_mode(const moe_shape& s, DispatchArgs a, cudaStream_
     }
     a.stages = stages;
     const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
-    int max_smem = 0;
-    cudaError_t e0 = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, 0);
-    if (e0 != cudaSuccess) return e0;
-    if (L.total > static_cast<size_t>(max_smem)) return cudaErrorInvalidConfiguration;
+    if (L.total > static_cast<size_t>(device_optin_smem())) return cudaErrorInvalidConfiguration;
     const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel<EXPERT>)
                            : reinterpret_cast<const void*>(dispatch_bf16_kernel<EXPERT>);
     const int threads = quant ? kInt8Threads : kBf16Threads;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(L.total));
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, L.total);
+    cudaError_t e = prepare_kernel(fn, L.total, threads, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;

@@ -168,11 +168,9 @@ cudaError_t launch_notify_expert(const moe_shape& s, const int32_t* topk_idx, co
     int32_t* ecount = static_cast<int32_t*>(scratch);
     cudaError_t e = cudaSuccess;
     if (p.chunks > 0) {
-        e = cudaFuncSetAttribute(expert_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(p.smem));
+        e = prepare_kernel(reinterpret_cast<const void*>(expert_count_kernel), p.smem, p.wpb * 32, nullptr);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(expert_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(p.smem));
+        e = prepare_kernel(reinterpret_cast<const void*>(expert_rows_kernel), p.smem, p.wpb * 32, nullptr);
         if (e != cudaSuccess) return e;
         e = launch_pdl(expert_count_kernel, static_cast<unsigned>(p.blocks), p.wpb * 32, p.smem, stream, s.E,
                        s.K, static_cast<int64_t>(s.S), p.chunks, topk_idx, ecount);

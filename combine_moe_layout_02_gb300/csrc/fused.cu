@@ -622,23 +622,15 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     a.ccT = reinterpret_cast<int32_t*>(sc + 256);
     a.ecount = a.ccT + a.PCp * s.P;
     a.err = err;
-    int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, fused_kernel);
-    if (e != cudaSuccess) return e;
-    int64_t limit = static_cast<int64_t>(optin) - static_cast<int64_t>(fa.sharedSizeBytes);
+    const int static_smem = kernel_static_smem(reinterpret_cast<const void*>(fused_kernel));
+    if (static_smem < 0) return cudaErrorInvalidDeviceFunction;
+    int64_t limit = static_cast<int64_t>(device_optin_smem()) - static_smem;
     if (limit > kSmemBudget) limit = kSmemBudget;
     size_t smem = 0;
     fused_plan(s, limit, &a.nb, &a.ab_off, &smem);
     if (a.nb < 1) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads, smem);
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(fused_kernel), smem, kThreads, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = device_sm_count();  // one CTA per SM: all resident (cooperative launch)

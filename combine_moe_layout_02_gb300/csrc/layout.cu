@@ -179,9 +179,7 @@ cudaError_t launch_layout(const moe_shape& s, const int32_t* topk_idx, int32_t* 
     const int64_t blocks = static_cast<int64_t>(s.P) * p.blocks_per_source;
     cudaError_t e = cudaSuccess;
     if (blocks > 0) {
-        e = cudaFuncSetAttribute(layout_count_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(p.smem));
+        e = prepare_kernel(reinterpret_cast<const void*>(layout_count_kernel), p.smem, p.threads, nullptr);
         if (e != cudaSuccess) return e;
         e = launch_pdl(layout_count_kernel, static_cast<unsigned>(blocks), p.threads, p.smem, stream, s.P,
                        s.E, s.K, static_cast<int64_t>(s.S / s.P), p.blocks_per_source, p.part_stride,

@@ -226,6 +226,14 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+// Opt-in shared memory per block of the current device (cached).
+int device_optin_smem();
+// Allow `fn` `smem` bytes of dynamic shared memory on the current device and,
+// if per_sm is given, return its resident blocks per SM for (threads, smem).
+// Both are cached per (kernel, device).
+cudaError_t prepare_kernel(const void* fn, size_t smem, int threads, int* per_sm);
+// Static shared memory of `fn` (cached), or -1.
+int kernel_static_smem(const void* fn);
 
 // Launch `kernel` on `stream` with programmatic stream serialisation (see
 // pdl_wait_then_release); the kernel must call pdl_wait_then_release before

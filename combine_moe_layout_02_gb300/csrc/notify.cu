@@ -355,11 +355,10 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
     int32_t* ccount = static_cast<int32_t*>(scratch);
     const size_t smem_count = p.rank_major ? 0 : static_cast<size_t>(p.wpb) * s.P * 4;
     const size_t smem_head = p.rank_major ? 0 : static_cast<size_t>(p.wpb + 1) * s.P * 4;
-    cudaError_t e = cudaFuncSetAttribute(notify_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_count));
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(notify_count_kernel), smem_count, p.threads,
+                                   nullptr);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(notify_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_head));
+    e = prepare_kernel(reinterpret_cast<const void*>(notify_head_kernel), smem_head, p.threads, nullptr);
     if (e != cudaSuccess) return e;
     const int64_t grid1 = p.chan_blocks + p.rank_blocks + p.expert_blocks;
     e = launch_pdl(notify_count_kernel, static_cast<unsigned>(grid1), p.threads, smem_count, stream, s.P,
