@@ -427,9 +427,6 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
-        // Routing words load while the row arrives and is quantised.
-        TokenRoute rt;
-        if constexpr (!EXPERT) rt = load_token_route(a, g, lane);
         const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>((i / NS) & 1));
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
@@ -475,7 +472,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                 int64_t rowi;
                 dst = expert_slot_of(a, prb, g, d, &rowi);
             } else {
-                const int32_t sh = d < 32 ? rt.sh0 : __ldg(a.send_head + g * a.P + d);
+                const int32_t sh = __ldg(a.send_head + g * a.P + d);
                 if (sh >= 0) dst = slot_of(a, prb, d, sh);
             }
             if (dst) {
@@ -490,7 +487,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         if constexpr (EXPERT)
             write_slot_meta(a, prb, g, lane);
         else
-            write_token_meta(a, prb, g, lane, rt);
+            write_token_meta(a, prb, g, lane, load_token_route(a, g, lane));
         if (spc >= 2) {
             // token i - kInt8Consumers (this warp's previous) has left its slot
             bulk_wait_read<1>();
