@@ -311,22 +311,47 @@ __device__ __forceinline__ int32_t quant_one(float x, float scale, float r, bool
 // even (IEEE round to nearest); the sum's low byte is then that integer mod 256.
 constexpr float kRoundMagic = 12582912.0f;
 
+// Packed binary32 pairs (two independent IEEE round-to-nearest operations per
+// instruction): the low word holds one element, the high word the next.
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f32x2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
 // 4 bf16 (two words) -> 4 int8 bytes of rint(x * r), with no conversion
-// instructions. `near` is set when some t = x * r lies within 2^-15 of a
-// half-integer, where rounding t may differ from rounding x / scale (see
-// quant_one); the caller then redoes the chunk with division.
+// instructions, two elements per arithmetic instruction. `near` is set when
+// some t = x * r lies within 2^-15 of a half-integer, where rounding t may
+// differ from rounding x / scale (see quant_one); the caller then redoes the
+// chunk with division.
 __device__ __forceinline__ uint32_t quant_fast4(uint32_t w0, uint32_t w1, float r, bool& near) {
-    const float x[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-    uint32_t b[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float t = __fmul_rn(x[i], r);
-        const float u = __fadd_rn(t, kRoundMagic);
-        const float d = __fsub_rn(t, __fsub_rn(u, kRoundMagic));
-        near |= fabsf(d) >= 0.5f - 0x1p-15f;
-        b[i] = __float_as_uint(u);
-    }
-    return __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+    const uint64_t rr = f32x2_pack(__float_as_uint(r), __float_as_uint(r));
+    const uint64_t mm = f32x2_pack(__float_as_uint(kRoundMagic), __float_as_uint(kRoundMagic));
+    const uint64_t t0 = f32x2_mul(f32x2_pack(w0 << 16, w0 & 0xffff0000u), rr);
+    const uint64_t t1 = f32x2_mul(f32x2_pack(w1 << 16, w1 & 0xffff0000u), rr);
+    const uint64_t u0 = f32x2_add(t0, mm), u1 = f32x2_add(t1, mm);
+    const uint64_t d0 = f32x2_sub(t0, f32x2_sub(u0, mm)), d1 = f32x2_sub(t1, f32x2_sub(u1, mm));
+    const float m = fmaxf(fmaxf(fabsf(f32x2_lo(d0)), fabsf(f32x2_hi(d0))),
+                          fmaxf(fabsf(f32x2_lo(d1)), fabsf(f32x2_hi(d1))));
+    near |= m >= 0.5f - 0x1p-15f;
+    const uint32_t lo = __byte_perm(static_cast<uint32_t>(u0), static_cast<uint32_t>(u0 >> 32), 0x0040);
+    const uint32_t hi = __byte_perm(static_cast<uint32_t>(u1), static_cast<uint32_t>(u1 >> 32), 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
 }
 
 // 8 bf16 (one 16-byte chunk) -> 8 int8, packed little-endian.
