@@ -74,8 +74,7 @@ struct DispatchSmem {
     size_t prb, bars, ring, total;
 };
 
-__host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes, int H,
-                                                      bool quant) {
+__host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes) {
     DispatchSmem l;
     l.prb = 0;
     l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
@@ -201,7 +200,7 @@ template <bool EXPERT>
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchArgs a) {
     pdl_wait_then_release();
     extern __shared__ __align__(128) unsigned char smem[];
-    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, false);
+    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     unsigned char* ring = smem + L.ring;
@@ -372,6 +371,14 @@ __device__ __forceinline__ uint2 quant_chunk(uint4 v, float scale, float r, bool
     return make_uint2(o[0], o[1]);
 }
 
+// The divisions of the int8 path (once per token, and per chunk only near a
+// half-integer) are out-of-line calls, so the registers of the hot loop are
+// not saved around them on every token.
+__device__ __noinline__ float scale_of_amax(float m) { return __fdiv_rn(m, 127.0f); }
+__device__ __noinline__ uint2 quant_chunk_exact(uint4 v, float scale, bool zero) {
+    return quant_chunk(v, scale, 0.f, false, zero);
+}
+
 // max |x| over 8 bf16, as a bf16 pair (bf16 max is exact).
 __device__ __forceinline__ __nv_bfloat162 absmax_chunk(__nv_bfloat162 m, uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -392,8 +399,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // (bulk loads completing on full[slot]) and reuses a slot once the consumer
 // that read it arrives on empty[slot]. Warps 1..kInt8Consumers each take
 // whole tokens in turn: amax by a warp reduction, scale = amax / 127, the
-// quantised row into the warp's own shared int8 row, then one bulk store per
-// destination, the scale block and the triple / side arrays. No block-wide
+// quantised row written in place over the front of its bf16 row in the slot,
+// then one bulk store per destination, the scale block and the triple / side
+// arrays; the slot is released once those stores have read it. No block-wide
 // barrier on the token path.
 template <bool EXPERT>
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     // 761 us at P=8, H=7168). The next kernel launches as these CTAs exit.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(128) unsigned char smem[];
-    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, a.H, true);
+    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kMaxStages;
@@ -462,7 +470,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         for (int j = lane; j < nchunks; j += 32) m2 = absmax_chunk(m2, row[j]);
         float m = fmaxf(__bfloat162float(m2.x), __bfloat162float(m2.y));
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float scale = __fdiv_rn(m, 127.0f);
+        const float scale = scale_of_amax(m);
         const bool zero = m == 0.f;
         const float r = zero ? 0.f : __frcp_rn(scale);
         const bool fast = !zero && isfinite(r);
@@ -480,9 +488,9 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                     bool near = false;
                     o.x = quant_fast4(v.x, v.y, r, near);
                     o.y = quant_fast4(v.z, v.w, r, near);
-                    if (near) o = quant_chunk(v, scale, r, false, false);
+                    if (near) o = quant_chunk_exact(v, scale, false);
                 } else {
-                    o = quant_chunk(v, scale, r, false, zero);
+                    o = quant_chunk_exact(v, scale, zero);
                 }
             }
             __syncwarp();
@@ -554,7 +562,7 @@ cudaError_t launch_dispatch_mode(const moe_shape& s, DispatchArgs a, cudaStream_
         stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
     }
     a.stages = stages;
-    const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, s.H, quant);
+    const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes);
     if (L.total > static_cast<size_t>(device_optin_smem())) return cudaErrorInvalidConfiguration;
     const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel<EXPERT>)
                            : reinterpret_cast<const void*>(dispatch_bf16_kernel<EXPERT>);
