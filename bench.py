@@ -297,7 +297,8 @@ def run_ours(args, world, rank, local):
     # made once here and every step's combine reads it.
     y_out, y_stride = None, None
     if w.quant:
-        rows_alloc = buf.expert_rows if expert else buf.arena_rows
+        # moe_run_host's arena (either layout) bounds the rows combine may read
+        rows_alloc = max(moe.moe_max_recv_rows(shape), moe.moe_max_expert_rows(shape))
         gen = torch.Generator(device=dev).manual_seed(0)
         y_out = torch.empty((max(rows_alloc, 1), w.H), dtype=torch.bfloat16, device=dev)
         y_out.normal_(generator=gen)
@@ -431,37 +432,22 @@ def run_ours(args, world, rank, local):
     h2d = x_host.numel() * 2 + idx_host.numel() * 4 + wts_host.numel() * 4
     d2h = out_host.numel() * 2
     e2e_steps = max(6, min(args.steps, 40))
-    if not expert:
-        # The serving call: moe_run_host streams the batches from pinned host
-        # memory through the path, overlapping the copies of neighbouring
-        # batches with compute (wall clock around the blocking call).
-        e2e_method = "moe_run_host: pinned host batches, 3-stream copy/compute overlap, wall clock"
-        ws_bytes = moe.moe_run_host_workspace_bytes(shape, e2e_steps)
-        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
-        hx, hi, hw, ho = [x_host] * e2e_steps, [idx_host] * e2e_steps, [wts_host] * e2e_steps, [out_host] * e2e_steps
-        moe.moe_run_host(shape, hx[:2], hi[:2], hw[:2], ho[:2], workspace, y=y_out, y_row_stride=y_stride or 0,
-                         fused=fused)  # warm-up
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        moe.moe_run_host(shape, hx, hi, hw, ho, workspace, y=y_out, y_row_stride=y_stride or 0, fused=fused)
-        e_elapsed = time.perf_counter() - t0
-        barrier(world)
-        del workspace
-    else:
-        e2e_method = "serial: copies in, entry points, copy out on one stream (CUDA events)"
-
-        def e2e_step():
-            x.copy_(x_host, non_blocking=True)
-            idx.copy_(idx_host, non_blocking=True)
-            wts.copy_(wts_host, non_blocking=True)
-            step()
-            out_host.copy_(out, non_blocking=True)
-
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e_elapsed = run_steps(e2e_steps, e2e_step)
-        barrier(world)
+    # The serving call: moe_run_host streams the batches from pinned host
+    # memory through the path, overlapping the copies of neighbouring batches
+    # with compute (wall clock around the blocking call).
+    e2e_method = "moe_run_host: pinned host batches, 3-stream copy/compute overlap, wall clock"
+    ws_bytes = moe.moe_run_host_workspace_bytes(shape, e2e_steps)
+    workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+    hx, hi, hw, ho = [x_host] * e2e_steps, [idx_host] * e2e_steps, [wts_host] * e2e_steps, [out_host] * e2e_steps
+    run_kw = dict(y=y_out, y_row_stride=y_stride or 0, fused=fused, expert=expert)
+    moe.moe_run_host(shape, hx[:2], hi[:2], hw[:2], ho[:2], workspace, **run_kw)  # warm-up
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    moe.moe_run_host(shape, hx, hi, hw, ho, workspace, **run_kw)
+    e_elapsed = time.perf_counter() - t0
+    barrier(world)
+    del workspace
     e_max, e_units = aggregate(e_elapsed, float(w.S * e2e_steps), world)
     if int(buf.err[0].item()) != 0:
         raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")

@@ -12,7 +12,7 @@
 //
 //   H2D stream:     [wait compute(i-2)] copy x, topk_idx, topk_weights -> slot i%2, record h2d(i)
 //   compute stream: [wait h2d(i), d2h(i-2)] layout, notify, dispatch, combine -> out slot i%2,
-//                   record compute(i)
+//                   record compute(i)   (or the expert-major calls, or fused -> combine)
 //   D2H stream:     [wait compute(i)] copy out slot i%2 -> host, record d2h(i)
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,9 +34,9 @@ struct RunBuffers {
     int32_t* idx[2];
     float* w[2];
     uint16_t* out[2];
-    int32_t *ntpr, *ntpe, *rpm, *cpm, *rcpm, *nrt, *nrtpe, *reo, *send_head, *errs;
+    int32_t *ntpr, *ntpe, *rpm, *cpm, *rcpm, *nrt, *nrtpe, *reo, *send_head, *errs, *slot_row;
     uint8_t* itr;
-    int64_t* prb;
+    int64_t *prb, *expert_part_base;
     void* arena;
     void* scratch;
     int64_t arena_rows, scratch_bytes, total;
@@ -68,7 +68,11 @@ RunBuffers carve(const moe_shape& s, int64_t n_batches, unsigned char* base) {
     b.reo = static_cast<int32_t*>(take(E * 4));
     b.send_head = static_cast<int32_t*>(take(S * P * 4));
     b.prb = static_cast<int64_t*>(take((P + 1) * 8));
-    b.arena_rows = moe_max_recv_rows(&s);
+    b.slot_row = static_cast<int32_t*>(take(S * K * 4));
+    b.expert_part_base = static_cast<int64_t*>(take((P + 1) * 8));
+    // One arena for either layout: rank-major rows or expert-major slots.
+    const int64_t rank_rows = moe_max_recv_rows(&s), expert_rows = moe_max_expert_rows(&s);
+    b.arena_rows = rank_rows > expert_rows ? rank_rows : expert_rows;
     b.arena = take(b.arena_rows * moe_slot_stride(s.H, s.quant));
     b.scratch_bytes = moe_scratch_bytes(&s);
     b.scratch = take(b.scratch_bytes);
@@ -125,7 +129,9 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
     moe_status st = moe_check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    if (n_batches < 0 || (flags & ~MOE_RUN_FUSED) != 0) return MOE_ERR_INVALID_ARG;
+    if (n_batches < 0 || (flags & ~(MOE_RUN_FUSED | MOE_RUN_EXPERT)) != 0) return MOE_ERR_INVALID_ARG;
+    // The fused launch builds the rank-major layout only.
+    if ((flags & MOE_RUN_FUSED) && (flags & MOE_RUN_EXPERT)) return MOE_ERR_INVALID_ARG;
     if (n_batches == 0) return MOE_OK;
     if (!x_host || !topk_idx_host || !out_host || !workspace || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
@@ -150,6 +156,7 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
     if (pl.init() != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(b.errs, 0, static_cast<size_t>(n_batches) * 4, pl.comp) != cudaSuccess) return MOE_ERR_CUDA;
     bool fused = (flags & MOE_RUN_FUSED) != 0;
+    const bool expert = (flags & MOE_RUN_EXPERT) != 0;
 
     for (int32_t i = 0; i < n_batches; ++i) {
         const int sl = i & 1;
@@ -185,11 +192,23 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
             st = moe_notify(&s, b.ntpr, b.ntpe, b.itr, b.rpm, b.cpm, b.rcpm, b.nrt, b.nrtpe, b.reo, b.send_head,
                             b.prb, b.scratch, b.scratch_bytes, pl.comp);
             if (st != MOE_OK) return st;
-            st = moe_dispatch(&s, b.x[sl], b.idx[sl], w, b.send_head, b.prb, b.arena, b.arena_rows, nullptr,
-                              nullptr, nullptr, err, pl.comp);
+            if (expert) {
+                st = moe_notify_expert(&s, b.idx[sl], b.nrtpe, b.reo, b.slot_row, b.expert_part_base, b.scratch,
+                                       b.scratch_bytes, pl.comp);
+                if (st != MOE_OK) return st;
+                st = moe_dispatch_expert(&s, b.x[sl], b.idx[sl], w, b.slot_row, b.expert_part_base, b.arena,
+                                         b.arena_rows, nullptr, nullptr, err, pl.comp);
+            } else {
+                st = moe_dispatch(&s, b.x[sl], b.idx[sl], w, b.send_head, b.prb, b.arena, b.arena_rows, nullptr,
+                                  nullptr, nullptr, err, pl.comp);
+            }
             if (st != MOE_OK) return st;
         }
-        st = moe_combine(&s, yy, ys, b.prb, b.arena_rows, b.send_head, b.idx[sl], w, b.out[sl], err, pl.comp);
+        if (expert)
+            st = moe_combine_expert(&s, yy, ys, b.expert_part_base, b.arena_rows, b.slot_row, b.idx[sl], w,
+                                    b.out[sl], err, pl.comp);
+        else
+            st = moe_combine(&s, yy, ys, b.prb, b.arena_rows, b.send_head, b.idx[sl], w, b.out[sl], err, pl.comp);
         if (st != MOE_OK) return st;
         if (cudaEventRecord(pl.comp_done[sl], pl.comp) != cudaSuccess) return MOE_ERR_CUDA;
 

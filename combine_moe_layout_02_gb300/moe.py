@@ -29,8 +29,9 @@ EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scrat
            "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused",
            "moe_run_host_workspace_bytes", "moe_run_host")
 
-# moe_run_host flag (include/moe.h).
+# moe_run_host flags (include/moe.h).
 MOE_RUN_FUSED = 1
+MOE_RUN_EXPERT = 2
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
 MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -287,7 +288,7 @@ def moe_run_host_workspace_bytes(shape: moe_shape, n_batches: int) -> int:
 
 
 def moe_run_host(shape: moe_shape, x_host, topk_idx_host, topk_weights_host, out_host, workspace,
-                 y=None, y_row_stride=0, fused=False, err_host=None):
+                 y=None, y_row_stride=0, fused=False, expert=False, err_host=None):
     """Run the path over len(x_host) host-resident batches end to end.
 
     x_host / topk_idx_host / out_host: sequences of host tensors (pinned for
@@ -314,7 +315,8 @@ def moe_run_host(shape: moe_shape, x_host, topk_idx_host, topk_weights_host, out
                             ctypes.cast(ids, ctypes.c_void_p),
                             ctypes.cast(ws, ctypes.c_void_p) if ws is not None else None,
                             ctypes.cast(outs, ctypes.c_void_p), _ptr(y), int(y_row_stride),
-                            MOE_RUN_FUSED if fused else 0, _ptr(workspace), workspace.numel(), eh)
+                            (MOE_RUN_FUSED if fused else 0) | (MOE_RUN_EXPERT if expert else 0), _ptr(workspace),
+                            workspace.numel(), eh)
     _check(st, "moe_run_host")
 
 

@@ -375,11 +375,14 @@ moe_status moe_layout_static_scratch(const moe_shape* shape, const int32_t* topk
  *                        result; entries may alias (batches are written back
  *                        in order)
  *   y, y_row_stride      expert outputs read by combine, device memory of at
- *                        least moe_max_recv_rows(shape) rows; NULL means
- *                        identity experts (combine reads the bf16 dispatch
- *                        arena, quant must be 0)
- *   flags                0, or MOE_RUN_FUSED: use moe_dispatch_fused when it
- *                        supports the shape (otherwise the separate calls)
+ *                        least max(moe_max_recv_rows, moe_max_expert_rows)
+ *                        rows; NULL means identity experts (combine reads the
+ *                        bf16 dispatch arena, quant must be 0)
+ *   flags                0 (rank-major layout), MOE_RUN_FUSED (use
+ *                        moe_dispatch_fused when it supports the shape,
+ *                        otherwise the separate calls) or MOE_RUN_EXPERT (the
+ *                        expert-major layout: moe_notify_expert,
+ *                        moe_dispatch_expert, moe_combine_expert); not both
  *   workspace            >= moe_run_host_workspace_bytes(shape, n_batches)
  *                        device bytes, 256-byte aligned, owned by the caller
  *   err_host             NULL or int32 [n_batches] host array: each batch's
@@ -388,6 +391,7 @@ moe_status moe_layout_static_scratch(const moe_shape* shape, const int32_t* topk
  * nonzero device error word in batch order.
  */
 #define MOE_RUN_FUSED 1
+#define MOE_RUN_EXPERT 2
 int64_t moe_run_host_workspace_bytes(const moe_shape* shape, int32_t n_batches);
 moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_t* const* x_host,
                         const int32_t* const* topk_idx_host, const float* const* topk_weights_host,

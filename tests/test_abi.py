@@ -99,7 +99,8 @@ def test_run_host_checks_arguments_on_the_host(lib):
 
     assert call(nb=0) == moe.MOE_OK                       # nothing to run
     assert call(nb=-1) == moe.MOE_ERR_INVALID_ARG
-    assert call(fl=2) == moe.MOE_ERR_INVALID_ARG          # unknown flag
+    assert call(fl=4) == moe.MOE_ERR_INVALID_ARG          # unknown flag
+    assert call(fl=moe.MOE_RUN_FUSED | moe.MOE_RUN_EXPERT) == moe.MOE_ERR_INVALID_ARG  # fused is rank-major
     assert call(wsb=need - 1) == moe.MOE_ERR_INVALID_ARG  # workspace too small
     assert call(wsp=ws + 16) == moe.MOE_ERR_INVALID_ARG   # workspace not 256-byte aligned
     assert call(x=None) == moe.MOE_ERR_INVALID_ARG

@@ -118,3 +118,30 @@ def test_fused_flag_falls_back_where_the_fused_kernel_does_not_apply():
     got = _run(ws, fused=True)
     for w, g in zip(ws, got):
         np.testing.assert_array_equal(g, _expected(w))
+
+
+def _expected_expert(w, weights=True):
+    lay, nt, _ = oracle.run_all(w.P, w.E, w.C, w.expert_alignment, w.H, 0, w.x_bits, w.topk_idx, w.topk_weights)
+    ex = oracle.notify_expert(w.P, w.E, w.topk_idx, nt["num_recv_tokens_per_expert"], nt["recv_expert_offset"])
+    rows = int(ex["expert_part_base"][-1])
+    dis = oracle.dispatch_expert(w.P, w.E, w.H, 0, w.x_bits, w.topk_idx, w.topk_weights, ex["slot_row"],
+                                 ex["expert_part_base"], rows)
+    ref = oracle.combine_expert(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0), ex["expert_part_base"],
+                                rows, ex["slot_row"], w.topk_idx, w.topk_weights if weights else None)
+    return ref["out"]
+
+
+def test_expert_major_batches_match_the_oracle():
+    import torch
+
+    ws = _batches(4, 16, 80, 256, 4, 3, mask_frac=0.1)
+    w0 = ws[0]
+    shape = moe.make_shape(w0.P, w0.E, w0.S, w0.K, w0.H, w0.C, w0.expert_alignment, 0)
+    xs = [torch.from_numpy(w.x_bits.view(np.int16)).pin_memory() for w in ws]
+    ids = [torch.from_numpy(w.topk_idx).pin_memory() for w in ws]
+    wts = [torch.from_numpy(w.topk_weights).pin_memory() for w in ws]
+    outs = [torch.empty((w0.S, w0.H), dtype=torch.int16).pin_memory() for _ in ws]
+    workspace = torch.empty((moe.moe_run_host_workspace_bytes(shape, 3),), dtype=torch.uint8, device="cuda")
+    moe.moe_run_host(shape, xs, ids, wts, outs, workspace, expert=True)
+    for w, o in zip(ws, outs):
+        np.testing.assert_array_equal(o.numpy().view(np.uint16), _expected_expert(w))
