@@ -109,3 +109,25 @@ def test_fused_refuses_large_shapes():
     with pytest.raises(moe.MoeError) as e:
         buf.dispatch_fused(x, idx, None)
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_fused_no_tokens():
+    """S = 0: every table is still written (zeros), nothing is copied, err 0."""
+    import torch
+
+    shape = moe.make_shape(4, 16, 0, 2, 64, 16, 1, 0)
+    buf = moe.Buffers(shape, "cuda")
+    x = torch.empty((0, 64), dtype=torch.int16, device="cuda")
+    idx = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    wts = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    for t in (buf.num_tokens_per_rank, buf.num_tokens_per_expert, buf.rank_prefix_matrix,
+              buf.num_recv_tokens, buf.num_recv_tokens_per_expert, buf.recv_expert_offset):
+        t.fill_(-5)
+    buf.part_row_base.fill_(-5)
+    buf.err.fill_(99)
+    buf.dispatch_fused(x, idx, wts)
+    torch.cuda.synchronize()
+    assert int(buf.err[0].item()) == 0
+    for t in (buf.num_tokens_per_rank, buf.num_tokens_per_expert, buf.rank_prefix_matrix,
+              buf.num_recv_tokens, buf.num_recv_tokens_per_expert, buf.recv_expert_offset, buf.part_row_base):
+        assert (t.cpu().numpy() == 0).all()

@@ -145,3 +145,17 @@ def test_expert_major_batches_match_the_oracle():
     moe.moe_run_host(shape, xs, ids, wts, outs, workspace, expert=True)
     for w, o in zip(ws, outs):
         np.testing.assert_array_equal(o.numpy().view(np.uint16), _expected_expert(w))
+
+
+def test_no_tokens_runs_and_reports_no_error():
+    import torch
+
+    shape = moe.make_shape(4, 16, 0, 2, 64)
+    empty_x = torch.empty((0, 64), dtype=torch.int16).pin_memory()
+    empty_i = torch.empty((0, 2), dtype=torch.int32).pin_memory()
+    out = torch.empty((0, 64), dtype=torch.int16).pin_memory()
+    workspace = torch.empty((moe.moe_run_host_workspace_bytes(shape, 2),), dtype=torch.uint8, device="cuda")
+    err = np.full(2, -1, np.int32)
+    for fused in (False, True):
+        moe.moe_run_host(shape, [empty_x] * 2, [empty_i] * 2, None, [out] * 2, workspace, fused=fused, err_host=err)
+        assert (err == 0).all()

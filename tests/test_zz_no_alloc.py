@@ -53,7 +53,9 @@ def test_static_scratch_layout_matches_moe_layout_twice():
              inputs.workload("p8_e256_t4096_h7168", with_x=False, seed=1)]
     for w in cases:
         shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0)
-        assert moe.moe_scratch_bytes(shape) <= moe.MOE_LAYOUT_STATIC_SCRATCH_BYTES
+        # Both shapes' layout partials fit the built-in buffer (the static call
+        # below would otherwise return MOE_ERR_UNSUPPORTED); moe_scratch_bytes is
+        # larger, as it also covers the other entry points' scratch.
         idx = torch.from_numpy(w.topk_idx).to(dev)
         ref = _outputs(shape, dev)
         scratch = torch.empty(moe.moe_scratch_bytes(shape), dtype=torch.uint8, device=dev)
