@@ -8,13 +8,12 @@
 // "一条 token 如何走完 MoE").
 //
 // Design (sm_103a): one thread per token, blocks never straddle source ranks.
-//  * Expert histogram: per k, __match_any_sync groups equal expert ids of the
-//    warp's 32 tokens and the group's leader adds the group size to the warp's
-//    private shared-memory histogram -- no atomics, one writer per address.
-//  * Rank counts: one __ballot_sync + __popc per rank over the warp's tokens.
-//  * Block totals: fixed-order sum over the warps' histograms; block partials
-//    go to scratch and a second kernel sums them in block order. Integer sums
-//    in a fixed order: the result is the same on every run.
+//  * Expert histogram: one shared-memory histogram per block, each (token, k)
+//    slot adds 1 with an integer atomic (the counts do not depend on the order).
+//  * Rank counts: one __ballot_sync + __popc per rank over the warp's tokens,
+//    summed over the block's warps in a fixed order.
+//  * Block partials go to scratch and a second kernel sums them in block
+//    order: the result is the same on every run.
 //  * The block's slice of is_token_in_rank (and of the packed bits) is built in
 //    shared memory and written out with 16-byte stores: the slice of rows
 //    [g0, g0+n) is one contiguous span.
@@ -34,7 +33,7 @@ __host__ __device__ inline LayoutSmem layout_smem(int P, int E, int tb) {
     const int nwarps = tb / 32;
     const int W = (P + 31) / 32;
     LayoutSmem l;
-    l.off_bits = static_cast<size_t>(round_up(static_cast<int64_t>(nwarps) * (P + E) * 4, 16));
+    l.off_bits = static_cast<size_t>(round_up((static_cast<int64_t>(nwarps) * P + E) * 4, 16));
     l.off_itr = l.off_bits + static_cast<size_t>(tb) * W * 4;
     l.total = l.off_itr + static_cast<size_t>(round_up(static_cast<int64_t>(tb) * P, 16));
     return l;
@@ -64,7 +63,7 @@ layout_count_kernel(int32_t P, int32_t E, int32_t K, int64_t T, int64_t nbs, int
     const int epr = E / P;
     const LayoutSmem L = layout_smem(P, E, tb);
     int32_t* hist_rank = reinterpret_cast<int32_t*>(smem);   // [nwarps][P]
-    int32_t* hist_exp = hist_rank + nwarps * P;               // [nwarps][E]
+    int32_t* hist_exp = hist_rank + nwarps * P;               // [E], whole block
     uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem + L.off_bits);  // [tb][W]
     uint8_t* tile_itr = smem + L.off_itr;                                   // [tb][P]
 
@@ -80,25 +79,19 @@ layout_count_kernel(int32_t P, int32_t E, int32_t K, int64_t T, int64_t nbs, int
     const bool active = tid < n;
     const int64_t g = g0 + tid;
     int bad = 0;
-    int32_t* my_hist = hist_exp + warp * E;
     uint8_t* my_row = tile_itr + tid * P;
     uint32_t* my_bits = tile_bits + tid * W;
     for (int k = 0; k < K; ++k) {
-        int32_t e = active ? __ldg(topk_idx + g * K + k) : -1;
-        if (e >= E) {
-            bad = 1;
-            e = -1;
-        }
-        if (e < 0) e = -1;
-        const uint32_t grp = __match_any_sync(0xffffffffu, e);
-        if (e >= 0) {
-            if (lane == __ffs(grp) - 1) my_hist[e] += __popc(grp);
+        const int32_t e = active ? __ldg(topk_idx + g * K + k) : -1;
+        if (e >= E) bad = 1;
+        if (e >= 0 && e < E) {
+            atomicAdd(hist_exp + e, 1);
             const int d = e / epr;
             my_row[d] = 1;
             my_bits[d >> 5] |= 1u << (d & 31);
         }
-        __syncwarp();
     }
+    __syncwarp();
     // Tokens of this warp per rank: one ballot per rank.
     for (int wd = 0; wd < W; ++wd) {
         const uint32_t word = my_bits[wd];
@@ -121,11 +114,7 @@ layout_count_kernel(int32_t P, int32_t E, int32_t K, int64_t T, int64_t nbs, int
         for (int w = 0; w < nwarps; ++w) sum += hist_rank[w * P + j];
         mine[j] = sum;
     }
-    for (int j = tid; j < E; j += tb) {
-        int32_t sum = 0;
-        for (int w = 0; w < nwarps; ++w) sum += hist_exp[w * E + j];
-        mine[P + j] = sum;
-    }
+    for (int j = tid; j < E; j += tb) mine[P + j] = hist_exp[j];
     if (tid == 0) mine[P + E] = any_bad;
 }
 

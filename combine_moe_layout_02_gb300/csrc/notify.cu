@@ -154,7 +154,7 @@ notify_count_kernel(int32_t P, int32_t E, int32_t C, int32_t A, int64_t T, bool 
             const int d = d0 + 4 * lane;
             if (d >= P) continue;
             int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-#pragma unroll 4
+#pragma unroll 8
             for (int64_t t = b; t < e; ++t) {
                 const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + (s * T + t) * P + d));
                 c0 += flag(w, 0);
@@ -243,6 +243,7 @@ notify_head_kernel(int32_t P, int32_t E, int32_t C, int64_t T, bool rank_major, 
             const int d = d0 + 4 * lane;
             if (d >= P) continue;
             int4 pre = make_int4(0, 0, 0, 0);
+#pragma unroll 4
             for (int64_t cc = 0; cc < c; ++cc) {
                 const int4 v = __ldg(reinterpret_cast<const int4*>(ccount + (s * C + cc) * P + d));
                 pre.x += v.x;
@@ -262,7 +263,7 @@ notify_head_kernel(int32_t P, int32_t E, int32_t C, int64_t T, bool rank_major, 
             rcpm[(static_cast<int64_t>(d + 1) * P + s) * C + c] = b1;
             rcpm[(static_cast<int64_t>(d + 2) * P + s) * C + c] = b2;
             rcpm[(static_cast<int64_t>(d + 3) * P + s) * C + c] = b3;
-#pragma unroll 4
+#pragma unroll 8
             for (int64_t t = b; t < e; ++t) {
                 const int64_t g = s * T + t;
                 const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + g * P + d));
