@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -222,7 +223,36 @@ def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int 
         passes += 1
     sample = (f"{name} ({layout} layout) with T={w.T} tokens per rank (S={w.S}, {passes} pass(es)); "
               "single-threaded oracle: layout+notify+dispatch+combine")
+    oracle_sample.last = dict(S=w.S, P=w.P, K=w.K, H=w.H, quant=w.quant, rows=rows, layout=layout)
     return w.S * passes / t_total, passes, t_total, sample
+
+
+def oracle_gbs(tokens_per_s):
+    """Algorithmic GB/s of the last oracle sample (the bench's byte formulas)."""
+    m = getattr(oracle_sample, "last", None)
+    if not m:
+        return None
+    if m["layout"] == "expert":
+        b = (dispatch_expert_bytes(m["S"], m["K"], m["H"], m["rows"], m["quant"])
+             + combine_expert_bytes(m["S"], m["K"], m["H"], m["rows"]))
+    else:
+        b = (dispatch_bytes(m["S"], m["P"], m["K"], m["H"], m["rows"], m["quant"])
+             + combine_bytes(m["S"], m["P"], m["K"], m["H"], m["rows"]))
+    return b / m["S"] * tokens_per_s / 1e9
+
+
+def host_info():
+    """Cores and CPU model of the machine the oracle runs on."""
+    info = {"nproc": os.cpu_count(), "machine": platform.machine()}
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                info["cpu"] = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return info
 
 
 def run_reference(args, world, rank):
@@ -248,7 +278,7 @@ def run_reference(args, world, rank):
         "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
                        fused=bool(args.fused), graph=bool(args.graph)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "GB_s": oracle_gbs(value), "host": host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -415,6 +445,7 @@ def run_ours(args, world, rank, local):
     t_front = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     t_disp = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     t_comb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    med = [statistics.median(e[a].elapsed_time(e[a + 1]) for e in evs) * 1e3 for a in range(3)]
     peak, peak_kind = measured_peaks()
     if expert:
         db = dispatch_expert_bytes(w.S, w.K, w.H, R, w.quant)
@@ -457,7 +488,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, passes, secs, sample = oracle_sample(args.workload, args.ref_tokens, args.cpu_seconds,
                                                   layout=args.layout)
-        cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+        cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+               "GB_s": oracle_gbs(tps), "host": host_info()}
 
     if rank != 0:
         return
@@ -486,6 +518,7 @@ def run_ours(args, world, rank, local):
                         "frac_of_8TBs": comb_gbs / 8000.0, "tokens_per_s": w.S / t_comb,
                         "bytes": cb},
             "recv_rows": R,
+            "median_us": {"layout_notify": med[0], "dispatch": med[1], "combine": med[2]},
         },
         "clocks": clk,
         "e2e": {"value": e_units / e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
