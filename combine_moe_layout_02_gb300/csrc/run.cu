@@ -143,6 +143,9 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
     // Combine reads the expert outputs y; without them (identity experts) it
     // reads the dispatch arena, which holds bf16 rows only.
     if (!y && s.quant != 0) return MOE_ERR_INVALID_ARG;
+    // y as moe_combine checks it, here before anything is enqueued.
+    if (y && (!aligned16(y) || y_row_stride < 2 * static_cast<int64_t>(s.H) || y_row_stride % 16 != 0))
+        return MOE_ERR_INVALID_ARG;
     const RunBuffers b = carve(s, n_batches, static_cast<unsigned char*>(workspace));
     if (workspace_bytes < b.total) return MOE_ERR_INVALID_ARG;
     const void* yy = y ? y : b.arena;

@@ -107,5 +107,8 @@ def test_run_host_checks_arguments_on_the_host(lib):
     q = moe.make_shape(4, 16, 64, 2, 64, quant=1)
     need_q = moe.moe_run_host_workspace_bytes(q, n)
     assert call(shape=q, wsb=need_q) == moe.MOE_ERR_INVALID_ARG  # int8 slots need expert outputs y
+    assert call(shape=q, wsb=need_q, y=1 << 20, ys=64) == moe.MOE_ERR_INVALID_ARG       # y rows shorter than 2H
+    assert call(shape=q, wsb=need_q, y=1 << 20, ys=136) == moe.MOE_ERR_INVALID_ARG      # stride not a multiple of 16
+    assert call(shape=q, wsb=need_q, y=(1 << 20) + 8, ys=128) == moe.MOE_ERR_INVALID_ARG  # y not 16-byte aligned
     holes = (ctypes.c_void_p * n)(1 << 20, None)
     assert call(o=holes) == moe.MOE_ERR_INVALID_ARG      # a batch without an output buffer
