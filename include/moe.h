@@ -26,6 +26,9 @@
  *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and returns; results are ready when the stream
  *     reaches them. Nothing synchronises with the host.
+ *   - The one exception to the two rules above is moe_run_host, the serving
+ *     loop: it takes HOST buffers for the batches, uses its own streams and
+ *     returns when the results are in host memory (see its declaration).
  *   - Arguments are validated on the host before anything is enqueued; a bad
  *     argument returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED and enqueues
  *     nothing. MOE_ERR_CUDA means a launch failed.
@@ -33,8 +36,9 @@
  *     partition or the arena, an inconsistent send_head) cannot be seen on the
  *     host. The kernels skip the offending element -- they never read or
  *     write out of bounds -- and store a moe_status code into the caller's
- *     device word `err` (may be NULL). moe_layout always writes `err` (0 or a
- *     code); the later calls only ever write a non-zero code into it.
+ *     device word `err` (may be NULL). moe_layout and moe_dispatch_fused
+ *     always write `err` (0 or a code); the other calls only ever write a
+ *     non-zero code into it.
  *   - Row-major layouts; int32 counts; the bf16 payload is passed as uint16
  *     bit patterns.
  *   - Alignment: every array pointer must be 16-byte aligned (the error word
