@@ -174,17 +174,28 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, kernel: str):
+def traffic_key(workload: str, T, layout: str):
+    """Key of a traffic record: the named workload at its own token count, with
+    ":expert" for the expert-major receive layout. None for any other token
+    count, which no record covers."""
+    from combine_moe_layout_02_gb300 import inputs
+
+    if T is not None and T != inputs.WORKLOADS[workload]["T"]:
+        return None
+    return workload + (":expert" if layout == "expert" else "")
+
+
+def recorded_traffic(key, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, when it was taken
     on the kernels as they are now."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if key is None or not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     if d.get("kernel_hash") != kernel_hash():
         return None
-    return d.get("per_launch_bytes", {}).get(workload, {}).get(kernel)
+    return d.get("per_launch_bytes", {}).get(key, {}).get(kernel)
 
 
 # --------------------------------------------------------------------------
@@ -457,8 +468,12 @@ def run_ours(args, world, rank, local):
     comb_gbs = cb / t_comb / 1e9
     dominant = "dispatch" if t_disp >= t_comb else "combine"
     ach = disp_gbs if dominant == "dispatch" else comb_gbs
-    kname = (("dispatch_int8_kernel" if w.quant else "dispatch_bf16_kernel") if dominant == "dispatch"
-             else "combine_kernel")
+    if dominant == "combine":
+        kname = "combine_kernel"
+    elif fused:
+        kname = "fused_kernel"  # layout + notify + dispatch in one launch
+    else:
+        kname = "dispatch_int8_kernel" if w.quant else "dispatch_bf16_kernel"
 
     # --- end to end through the public API with host buffers -------------
     h2d = x_host.numel() * 2 + idx_host.numel() * 4 + wts_host.numel() * 4
@@ -507,7 +522,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": (3 if args.fused else (9 if expert else 6)) * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
-                     "traffic": recorded_traffic(args.workload, kname),
+                     "traffic": recorded_traffic(traffic_key(args.workload, args.tokens_per_rank, args.layout),
+                                                 kname),
                      "algorithmic_bytes": db if dominant == "dispatch" else cb},
         "stages": {
             "layout_notify_us": 1e6 * t_front,
