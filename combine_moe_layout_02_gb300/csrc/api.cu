@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe.h"
@@ -10,27 +11,33 @@
 
 namespace moe {
 
-int device_sm_count() {
-    static int cached[64] = {0};
+namespace {
+
+// A device attribute, cached per device (0 = not read yet). Threads that race
+// on a first read store the same value.
+int cached_attribute(std::atomic<int> (&cache)[64], cudaDeviceAttr attr, int fallback) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-    int n = 1;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n < 1) n = 1;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fallback;
+    const bool slot = dev >= 0 && dev < 64;
+    if (slot) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess || n < 1) return fallback;
+    if (slot) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
+std::atomic<int> g_sm_count[64];
+std::atomic<int> g_optin_smem[64];
+
+}  // namespace
+
+int device_sm_count() { return cached_attribute(g_sm_count, cudaDevAttrMultiProcessorCount, 1); }
+
 int device_optin_smem() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 48 * 1024;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-    int n = 48 * 1024;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (dev >= 0 && dev < 64) cached[dev] = n;
-    return n;
+    return cached_attribute(g_optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, 48 * 1024);
 }
 
 namespace {
@@ -146,6 +153,10 @@ moe_status moe_check_shape(const moe_shape* s) {
     if (s->num_channels > 4096) return MOE_ERR_UNSUPPORTED;
     if (s->H % 8 != 0) return MOE_ERR_INVALID_ARG;
     if (s->quant && s->H % 16 != 0) return MOE_ERR_INVALID_ARG;
+    // Row counts and offsets are int32: the expert-major bound on one rank's
+    // rows, S*K + E*(expert_alignment-1), must fit.
+    if (static_cast<int64_t>(s->S) * s->K + static_cast<int64_t>(s->E) * (s->expert_alignment - 1) > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 

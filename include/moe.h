@@ -72,6 +72,8 @@ typedef enum moe_status {
 #define MOE_MAX_EXPERTS 4096
 #define MOE_MAX_TOPK 16
 #define MOE_MAX_HIDDEN 16384
+/* Also S*K + E*(expert_alignment-1) <= INT32_MAX, so that every per-rank row
+ * count and offset fits int32; larger shapes return MOE_ERR_UNSUPPORTED. */
 
 /* Shape of one call. The tiling record of "HCCL Window 模式 (Non-SHMEM)
  * 代码深度剖析", section 8.1 (epWorldSize, moeExpertNum, quantMode, bs, k, h)

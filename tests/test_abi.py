@@ -52,6 +52,10 @@ def test_slot_stride_and_limits(lib):
     assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 8, 7176, quant=1)) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_check_shape(moe.make_shape(2048, 4096, 2048, 8, 64)) == moe.MOE_ERR_UNSUPPORTED
     assert moe.moe_check_shape(moe.make_shape(8, 256, 0, 8, 7168)) == moe.MOE_OK
+    # row counts are int32: S*K + E*(alignment-1) must fit
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 8, 7168, expert_alignment=8_000_000)) == moe.MOE_OK
+    assert moe.moe_check_shape(moe.make_shape(8, 256, 32768, 8, 7168,
+                                              expert_alignment=8_388_608)) == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_null_pointers_rejected_before_any_launch(lib):
