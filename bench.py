@@ -206,30 +206,49 @@ def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int 
     """Time the oracle's full path on a bounded sample of the workload: the same
     shape with T_sample tokens per rank. Returns tokens/s, passes, seconds and
     a description of the sample."""
+    import numpy as np
+
     import oracle
     from combine_moe_layout_02_gb300 import inputs
 
     w = workload if workload is not None else inputs.workload(name, T=T_sample)
-    passes, t_total = 0, 0.0
-    while passes < max_passes and (passes == 0 or t_total < min_seconds):
-        t0 = time.perf_counter()
+    expert = layout == "expert"
+
+    def front():
         lay = oracle.layout(w.P, w.E, w.topk_idx)
         nt = oracle.notify(w.P, w.E, w.C, w.expert_alignment, lay["num_tokens_per_rank"],
                            lay["num_tokens_per_expert"], lay["is_token_in_rank"])
-        if layout == "expert":
-            ex = oracle.notify_expert(w.P, w.E, w.topk_idx, nt["num_recv_tokens_per_expert"],
-                                      nt["recv_expert_offset"])
+        ex = (oracle.notify_expert(w.P, w.E, w.topk_idx, nt["num_recv_tokens_per_expert"],
+                                   nt["recv_expert_offset"]) if expert else None)
+        return nt, ex
+
+    # int8 slots: combine reads bf16 expert outputs, which the path does not
+    # make. As in the GPU arm, one seeded bf16 arena of the received rows stands
+    # in for them; it is drawn once, outside the timed passes.
+    y_int8 = None
+    if w.quant:
+        nt, ex = front()
+        rows = int((ex["expert_part_base"] if expert else nt["part_row_base"])[-1])
+        y_int8 = inputs.draw_hidden(max(rows, 1), w.H, np.random.default_rng(1))
+    passes, t_total = 0, 0.0
+    while passes < max_passes and (passes == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        nt, ex = front()
+        if expert:
             rows = int(ex["expert_part_base"][-1])
             dis = oracle.dispatch_expert(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
                                          ex["slot_row"], ex["expert_part_base"], rows)
-            oracle.combine_expert(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0),
-                                  ex["expert_part_base"], rows, ex["slot_row"], w.topk_idx, w.topk_weights)
         else:
             rows = int(nt["part_row_base"][-1])
             dis = oracle.dispatch(w.P, w.E, w.H, w.quant, w.x_bits, w.topk_idx, w.topk_weights,
                                   nt["send_head"], nt["part_row_base"], rows)
-            oracle.combine(w.P, w.E, w.H, dis["arena"], oracle.slot_stride(w.H, 0), nt["part_row_base"],
-                           rows, nt["send_head"], w.topk_idx, w.topk_weights)
+        y, y_stride = (y_int8, 2 * w.H) if w.quant else (dis["arena"], oracle.slot_stride(w.H, 0))
+        if expert:
+            oracle.combine_expert(w.P, w.E, w.H, y, y_stride, ex["expert_part_base"], rows, ex["slot_row"],
+                                  w.topk_idx, w.topk_weights)
+        else:
+            oracle.combine(w.P, w.E, w.H, y, y_stride, nt["part_row_base"], rows, nt["send_head"], w.topk_idx,
+                           w.topk_weights)
         t_total += time.perf_counter() - t0
         passes += 1
     sample = (f"{name} ({layout} layout) with T={w.T} tokens per rank (S={w.S}, {passes} pass(es)); "

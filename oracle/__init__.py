@@ -176,11 +176,21 @@ def dispatch(P: int, E: int, H: int, quant: int, x_bits: np.ndarray, topk_idx: n
     return out
 
 
+def _check_rows(y: np.ndarray, y_row_stride: int, arena_rows: int, H: int) -> None:
+    """The C oracle reads ``arena_rows`` rows of ``2*H`` bytes ``y_row_stride``
+    apart from ``y``; refuse a ``y`` that does not hold them."""
+    if y_row_stride < 2 * H:
+        raise ValueError(f"y_row_stride {y_row_stride} < 2*H = {2 * H}")
+    if arena_rows > 0 and y.size < (arena_rows - 1) * y_row_stride + 2 * H:
+        raise ValueError(f"y holds {y.size} bytes, fewer than {arena_rows} rows of stride {y_row_stride}")
+
+
 def combine(P: int, E: int, H: int, y: np.ndarray, y_row_stride: int, part_row_base: np.ndarray,
             arena_rows: int, send_head: np.ndarray, topk_idx: np.ndarray,
             topk_weights: np.ndarray | None, tokens: np.ndarray | None = None) -> dict:
     """Run the combine oracle; ``y`` is the raw byte arena (rows y_row_stride apart)."""
     y = np.ascontiguousarray(y).view(np.uint8)
+    _check_rows(y, y_row_stride, arena_rows, H)
     send_head = _c(send_head, np.int32)
     topk_idx = _c(topk_idx, np.int32)
     w = None if topk_weights is None else _c(topk_weights, np.float32)
@@ -229,6 +239,7 @@ def dispatch_expert(P: int, E: int, H: int, quant: int, x_bits, topk_idx, topk_w
 def combine_expert(P: int, E: int, H: int, y, y_row_stride: int, expert_part_base, arena_rows: int,
                    slot_row, topk_idx, topk_weights, tokens=None) -> dict:
     y = np.ascontiguousarray(y).view(np.uint8)
+    _check_rows(y, y_row_stride, arena_rows, H)
     idx = _c(topk_idx, np.int32)
     S, K = idx.shape
     w = None if topk_weights is None else _c(topk_weights, np.float32)
