@@ -24,11 +24,11 @@
 //  * int8: a producer warp streams rows into the ring (full / empty
 //    mbarriers); consumer warps each take whole tokens: amax by a warp
 //    reduction, quantisation (exact round-half-even of x / scale, see
-//    quant_one and quant_fast4) written in place over the front of the bf16
-//    row in its ring slot, then the same bulk stores fan that row out. The
-//    slot goes back to the producer once those stores have read it. Small
-//    rings (one slot per consumer) and few consumers per CTA, so many CTAs
-//    -- and so many quantising warps -- share an SM.
+//    quant_one and quant_fast4) into the warp's own int8 row buffer, after
+//    which the ring slot goes straight back to the producer; the same bulk
+//    stores then fan the int8 row out. One slot per consumer and three
+//    consumers per CTA, so several CTAs -- and so many quantising warps --
+//    share an SM.
 // Every mbarrier wait is bounded; on time-out the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains its own copies (bounded) and returns.
 #include <cuda_bf16.h>
@@ -49,10 +49,10 @@
 #endif
 // int8 dispatch: ring budget and number of quantising (consumer) warps per CTA.
 #ifndef MOE_DISPATCH_INT8_RING_BYTES
-#define MOE_DISPATCH_INT8_RING_BYTES (32 * 1024)
+#define MOE_DISPATCH_INT8_RING_BYTES (48 * 1024)
 #endif
 #ifndef MOE_DISPATCH_INT8_CONSUMERS
-#define MOE_DISPATCH_INT8_CONSUMERS 2
+#define MOE_DISPATCH_INT8_CONSUMERS 3
 #endif
 
 namespace moe {
@@ -71,17 +71,20 @@ static_assert(kStoreDepth >= 1 && kStoreDepth < kMaxStages, "store depth must le
 static_assert(kMaxStages >= kInt8Consumers, "the int8 ring needs a slot per consumer warp");
 
 struct DispatchSmem {
-    size_t prb, bars, ring, total;
+    size_t prb, bars, ring, qbuf, qstride, total;
 };
 
-__host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes) {
+// qbuf: an int8 row buffer for each int8 consumer warp after the ring
+// (row_bytes / 2 bytes, rounded up to 128); none for the bf16 kernel.
+__host__ __device__ inline DispatchSmem dispatch_smem(int P, int stages, uint32_t row_bytes, bool qbuf = false) {
     DispatchSmem l;
     l.prb = 0;
     l.bars = static_cast<size_t>(round_up(static_cast<int64_t>(P + 1) * 8, 128));
     // full[kMaxStages] then empty[kMaxStages] (the bf16 kernel uses full only)
     l.ring = l.bars + static_cast<size_t>(round_up(2 * kMaxStages * 8, 128));
-    // int8 rows are written in place over their bf16 source in the ring
-    l.total = l.ring + static_cast<size_t>(stages) * row_bytes;
+    l.qbuf = l.ring + static_cast<size_t>(stages) * row_bytes;
+    l.qstride = qbuf ? static_cast<size_t>(round_up(row_bytes / 2, 128)) : 0;
+    l.total = l.qbuf + static_cast<size_t>(kInt8Consumers) * l.qstride;
     return l;
 }
 
@@ -399,10 +402,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // (bulk loads completing on full[slot]) and reuses a slot once the consumer
 // that read it arrives on empty[slot]. Warps 1..kInt8Consumers each take
 // whole tokens in turn: amax by a warp reduction, scale = amax / 127, the
-// quantised row written in place over the front of its bf16 row in the slot,
-// then one bulk store per destination, the scale block and the triple / side
-// arrays; the slot is released once those stores have read it. No block-wide
-// barrier on the token path.
+// quantised row written to the warp's own int8 row buffer, the slot handed
+// back to the producer, then one bulk store per destination from the row
+// buffer, the scale block and the triple / side arrays. The next row's load
+// thus overlaps this row's stores; the row buffer is rewritten once those
+// stores have read it. No block-wide barrier on the token path.
 template <bool EXPERT>
 __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const DispatchArgs a) {
     // Waits for the previous kernel but does not let the next one be scheduled
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     // 761 us at P=8, H=7168). The next kernel launches as these CTAs exit.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(128) unsigned char smem[];
-    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes);
+    const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, true);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kMaxStages;
@@ -455,8 +459,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
 
     const int cw = warp - 1;
     const int nchunks = a.H / 8;
-    const int spc = NS / kInt8Consumers;  // ring slots per consumer
-    int64_t last_i = -1;
+    unsigned char* q = smem + L.qbuf + static_cast<size_t>(cw) * L.qstride;  // this warp's int8 row
     for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
@@ -467,6 +470,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         }
         const uint4* row = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * RB);
         __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+#pragma unroll 4
         for (int j = lane; j < nchunks; j += 32) m2 = absmax_chunk(m2, row[j]);
         float m = fmaxf(__bfloat162float(m2.x), __bfloat162float(m2.y));
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -474,16 +478,14 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         const bool zero = m == 0.f;
         const float r = zero ? 0.f : __frcp_rn(scale);
         const bool fast = !zero && isfinite(r);
-        // In place: the int8 row overwrites the front of the ring slot. Chunk j's
-        // 8 bytes land in bf16 chunks j/2, already read (syncwarp between the
-        // reads and writes of one iteration).
-        unsigned char* q = const_cast<unsigned char*>(reinterpret_cast<const unsigned char*>(row));
+        // The previous token's stores have read the row buffer.
+        bulk_wait_read<0>();
+        __syncwarp();
         for (int j0 = 0; j0 < nchunks; j0 += 32) {
             const int j = j0 + lane;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (j < nchunks) v = row[j];
-            uint2 o = make_uint2(0, 0);
             if (j < nchunks) {
+                const uint4 v = row[j];
+                uint2 o;
                 if (fast) {
                     bool near = false;
                     o.x = quant_fast4(v.x, v.y, r, near);
@@ -492,10 +494,13 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
                 } else {
                     o = quant_chunk_exact(v, scale, zero);
                 }
+                reinterpret_cast<uint2*>(q)[j] = o;
             }
-            __syncwarp();
-            if (j < nchunks) reinterpret_cast<uint2*>(q)[j] = o;
         }
+        // Every lane has read the bf16 row: the slot goes back to the producer
+        // now, so the next load overlaps this token's stores.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
         fence_proxy_async_smem();
         __syncwarp();
         const int nfan = EXPERT ? a.K : a.P;
@@ -521,22 +526,6 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
             write_slot_meta(a, prb, g, lane);
         else
             write_token_meta(a, prb, g, lane, load_token_route(a, g, lane));
-        if (spc >= 2) {
-            // token i - kInt8Consumers (this warp's previous) has left its slot
-            bulk_wait_read<1>();
-            __syncwarp();
-            if (lane == 0 && i >= kInt8Consumers) mbar_arrive(&empty[(i - kInt8Consumers) % NS]);
-        } else {
-            bulk_wait_read<0>();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-        last_i = i;
-    }
-    if (spc >= 2 && last_i >= 0) {
-        bulk_wait_read<0>();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[last_i % NS]);
     }
     bulk_wait<0>();
 }
@@ -562,7 +551,7 @@ cudaError_t launch_dispatch_mode(const moe_shape& s, DispatchArgs a, cudaStream_
         stages = stages < min_stages ? min_stages : (stages > kMaxStages ? kMaxStages : stages);
     }
     a.stages = stages;
-    const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes);
+    const DispatchSmem L = dispatch_smem(s.P, stages, a.row_bytes, quant);
     if (L.total > static_cast<size_t>(device_optin_smem())) return cudaErrorInvalidConfiguration;
     const void* fn = quant ? reinterpret_cast<const void*>(dispatch_int8_kernel<EXPERT>)
                            : reinterpret_cast<const void*>(dispatch_bf16_kernel<EXPERT>);

@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
@@ -57,13 +58,19 @@ def make_shape(P, E, S, K, H, num_channels=16, expert_alignment=1, quant=0) -> m
 
 
 _lib = None
+_lib_lock = threading.Lock()
 
 
 def lib() -> ctypes.CDLL:
     """Open libmoe.so (raises if it is missing)."""
-    global _lib
     if _lib is not None:
         return _lib
+    with _lib_lock:
+        return _lib if _lib is not None else _open_lib()
+
+
+def _open_lib() -> ctypes.CDLL:
+    global _lib
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
     try:  # torch's CUDA runtime satisfies libmoe's libcudart dependency
