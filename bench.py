@@ -201,13 +201,32 @@ def recorded_traffic(key, kernel: str):
 # --------------------------------------------------------------------------
 # CPU oracle on a bounded sample (reference arm and cpu_baseline).
 
+def int8_stand_in(w, layout: str):
+    """bf16 rows standing in for the expert outputs an int8 combine reads: one
+    seeded N(0,1) row per received row of the workload (the path makes no bf16
+    rows for int8 slots; the GPU arm uses such an arena too)."""
+    import numpy as np
+
+    import oracle
+    from combine_moe_layout_02_gb300 import inputs
+
+    lay = oracle.layout(w.P, w.E, w.topk_idx)
+    nt = oracle.notify(w.P, w.E, w.C, w.expert_alignment, lay["num_tokens_per_rank"],
+                       lay["num_tokens_per_expert"], lay["is_token_in_rank"])
+    if layout == "expert":
+        ex = oracle.notify_expert(w.P, w.E, w.topk_idx, nt["num_recv_tokens_per_expert"],
+                                  nt["recv_expert_offset"])
+        rows = int(ex["expert_part_base"][-1])
+    else:
+        rows = int(nt["part_row_base"][-1])
+    return inputs.draw_hidden(max(rows, 1), w.H, np.random.default_rng(1))
+
+
 def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int = 1000,
-                  workload=None, layout: str = "rank"):
+                  workload=None, layout: str = "rank", y_int8=None):
     """Time the oracle's full path on a bounded sample of the workload: the same
     shape with T_sample tokens per rank. Returns tokens/s, passes, seconds and
     a description of the sample."""
-    import numpy as np
-
     import oracle
     from combine_moe_layout_02_gb300 import inputs
 
@@ -222,14 +241,10 @@ def oracle_sample(name: str, T_sample: int, min_seconds: float, max_passes: int 
                                    nt["recv_expert_offset"]) if expert else None)
         return nt, ex
 
-    # int8 slots: combine reads bf16 expert outputs, which the path does not
-    # make. As in the GPU arm, one seeded bf16 arena of the received rows stands
-    # in for them; it is drawn once, outside the timed passes.
-    y_int8 = None
-    if w.quant:
-        nt, ex = front()
-        rows = int((ex["expert_part_base"] if expert else nt["part_row_base"])[-1])
-        y_int8 = inputs.draw_hidden(max(rows, 1), w.H, np.random.default_rng(1))
+    # int8 slots: combine reads bf16 expert outputs (int8_stand_in), drawn
+    # outside the timed passes when the caller has not drawn them already.
+    if w.quant and y_int8 is None:
+        y_int8 = int8_stand_in(w, layout)
     passes, t_total = 0, 0.0
     while passes < max_passes and (passes == 0 or t_total < min_seconds):
         t0 = time.perf_counter()
@@ -291,12 +306,14 @@ def run_reference(args, world, rank):
     from combine_moe_layout_02_gb300 import inputs
 
     w = inputs.workload(args.workload, T=args.ref_tokens)
+    y_int8 = int8_stand_in(w, args.layout) if w.quant else None  # drawn once, untimed
     for _ in range(args.warmup):
-        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w, layout=args.layout)
+        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w, layout=args.layout,
+                      y_int8=y_int8)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         _, _, _, sample = oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w,
-                                        layout=args.layout)
+                                        layout=args.layout, y_int8=y_int8)
     elapsed = time.perf_counter() - t0
     value = w.S * args.steps / elapsed
     sample = sample.replace("1 pass(es)", f"{args.steps} timed steps of 1 pass")
