@@ -320,7 +320,7 @@ def run_reference(args, world, rank):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(w.quant),
         "data": "synthetic",
         "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
                        fused=bool(args.fused), graph=bool(args.graph)),
@@ -329,6 +329,12 @@ def run_reference(args, world, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def path_dtype(quant: int) -> str:
+    """What the path moves and computes in: bf16 rows (fp32 accumulation in
+    combine), or int8 rows quantised in fp32 from bf16 with an fp32 scale."""
+    return "int8" if quant else "bf16"
 
 
 def workload_config(name, T=None):
@@ -547,7 +553,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(w.quant), "data": "synthetic",
         "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
                        fused=bool(args.fused), graph=bool(args.graph),
                        l2=("no flush: working set (x, receive arena, out) of "
