@@ -47,6 +47,8 @@
 // lives in scratch and is zeroed by a one-thread kernel launched just before
 // (both launches use programmatic dependent launch, so the fused kernel is
 // scheduled while earlier work drains); err is cleared by the kernel itself.
+#include <atomic>
+
 #include "moe_device.cuh"
 
 namespace moe {
@@ -550,6 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const FusedArgs a) {
 
 // Row buffers per warp, the offset of the phase A / B region and the dynamic
 // shared memory of the launch, for a budget of `limit` bytes.
+// Per device: 0 = not tried yet, 1 = cooperative + programmatic serialisation
+// accepted, 2 = refused.
+std::atomic<int> g_coop_pdl[64];
+
 void fused_plan(const moe_shape& s, int64_t limit, int* nb, uint32_t* ab_off, size_t* smem) {
     const int64_t pc = static_cast<int64_t>(s.P) * s.num_channels;
     const int64_t a = static_cast<int64_t>(kWarps) * s.E * 4;
@@ -647,11 +653,26 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, fused_kernel, a);
-    if (e == cudaSuccess) return e;
-    // Without programmatic serialisation the launch simply follows the prep kernel.
-    (void)cudaGetLastError();
+    // Whether this device takes a cooperative launch with programmatic
+    // serialisation is learnt on the first call and remembered, so a refusal is
+    // not paid again on every call. Without it the launch simply follows the
+    // prep kernel.
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool slot = dev >= 0 && dev < 64;
+    const int known = slot ? g_coop_pdl[dev].load(std::memory_order_relaxed) : 0;
+    if (known != 2) {
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, fused_kernel, a);
+        if (e == cudaSuccess) {
+            if (slot) g_coop_pdl[dev].store(1, std::memory_order_relaxed);
+            return e;
+        }
+        if (known == 1) return e;  // it worked before: a real error
+        (void)cudaGetLastError();
+        if (slot) g_coop_pdl[dev].store(2, std::memory_order_relaxed);
+    }
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fused_kernel, a);
 }
