@@ -31,6 +31,7 @@ int cached_attribute(std::atomic<int> (&cache)[64], cudaDeviceAttr attr, int fal
 
 std::atomic<int> g_sm_count[64];
 std::atomic<int> g_optin_smem[64];
+std::atomic<int> g_sm_smem[64];
 
 }  // namespace
 
@@ -38,6 +39,10 @@ int device_sm_count() { return cached_attribute(g_sm_count, cudaDevAttrMultiProc
 
 int device_optin_smem() {
     return cached_attribute(g_optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, 48 * 1024);
+}
+
+int device_sm_smem() {
+    return cached_attribute(g_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, 64 * 1024);
 }
 
 namespace {

@@ -68,6 +68,12 @@ constexpr int kSumUnroll = 16;
 // Dynamic shared memory a CTA may use next to the kernel's static shared
 // memory (sm_100-class opt-in limit 227 KB, less a margin for static data).
 constexpr int kSmemBudget = 227 * 1024 - 1024;
+// CTAs per SM tried first; a shape whose row buffers do not fit in that share
+// of the SM's shared memory runs one CTA per SM.
+#ifndef MOE_FUSED_CTAS_PER_SM
+#define MOE_FUSED_CTAS_PER_SM 2
+#endif
+constexpr int kCtasPerSm = MOE_FUSED_CTAS_PER_SM;
 
 struct FusedArgs {
     int32_t P, E, K, H, C, A, epr, nb;
@@ -506,7 +512,7 @@ __global__ void fused_prep_kernel(unsigned int* counter) {
     if (threadIdx.x == 0) *counter = 0u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_kernel(const FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait_then_release();
     __shared__ int64_t prb[kMaxP + 1];
@@ -633,13 +639,23 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     int64_t limit = static_cast<int64_t>(device_optin_smem()) - static_smem;
     if (limit > kSmemBudget) limit = kSmemBudget;
     size_t smem = 0;
-    fused_plan(s, limit, &a.nb, &a.ab_off, &smem);
+    int cps = 1;
+    if (kCtasPerSm > 1) {
+        // Each CTA's share of the SM's shared memory, less the per-CTA reservation.
+        int64_t share = static_cast<int64_t>(device_sm_smem()) / kCtasPerSm - 1024 - static_smem;
+        if (share > limit) share = limit;
+        fused_plan(s, share, &a.nb, &a.ab_off, &smem);
+        if (a.nb >= 1) cps = kCtasPerSm;
+    }
+    if (cps == 1) fused_plan(s, limit, &a.nb, &a.ab_off, &smem);
     if (a.nb < 1) return cudaErrorInvalidConfiguration;
     int per_sm = 0;
     cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(fused_kernel), smem, kThreads, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const int grid = device_sm_count();  // one CTA per SM: all resident (cooperative launch)
+    if (per_sm < cps) cps = per_sm;
+    // cps CTAs per SM, all resident at once (cooperative launch).
+    const int grid = device_sm_count() * cps;
     e = launch_pdl(fused_prep_kernel, 1, 32, 0, stream, a.barrier);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -228,6 +228,8 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
 int device_sm_count();
 // Opt-in shared memory per block of the current device (cached).
 int device_optin_smem();
+// Shared memory of one SM (all its CTAs together), per current device.
+int device_sm_smem();
 // Allow `fn` `smem` bytes of dynamic shared memory on the current device and,
 // if per_sm is given, return its resident blocks per SM for (threads, smem).
 // Both are cached per (kernel, device).
