@@ -239,9 +239,10 @@ moe_status moe_combine(const moe_shape* shape, const void* y, int64_t y_row_stri
  * meaning, layout and value of the three separate calls with packed partitions
  * (part_row_base is written here and used for the rows).
  *
- * One cooperative persistent kernel (one CTA per SM) with two bounded grid
- * barriers; the barrier counter lives in scratch and is zeroed by a one-thread
- * kernel launched on the stream just before. `err` is always written: cleared by the kernel, then
+ * One cooperative persistent kernel (two CTAs per SM when their row buffers
+ * fit in half an SM's shared memory, else one) with two bounded grid barriers;
+ * the barrier counter lives in scratch and is zeroed by a one-thread kernel
+ * launched on the stream just before. `err` is always written: cleared by the kernel, then
  * raised to MOE_ERR_TOPK_OUT_OF_RANGE, MOE_ERR_CAPACITY or
  * MOE_ERR_DEVICE_TIMEOUT if needed.
  * Supported: P <= 64, E <= 1024, H <= 8192, K <= 16, P * num_channels <= 4096,
