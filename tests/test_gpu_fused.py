@@ -60,7 +60,8 @@ def test_fused_tiny():
 
 
 @pytest.mark.parametrize("name,T", [("p32_e256_t128_h1024", None), ("p32_e256_t128_h7168", None),
-                                    ("p8_e256_t4096_h7168", 300), ("p32_e256_t128_h2048", 37)])
+                                    ("p32_e256_t128_h4096", None), ("p8_e256_t4096_h7168", 300),
+                                    ("p8_e256_t4096_h7168", None), ("p32_e256_t128_h2048", 37)])
 def test_fused_workloads(name, T):
     _check_fused(inputs.workload(name, T=T), sample=600 if T is None else None)
 
