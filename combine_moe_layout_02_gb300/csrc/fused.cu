@@ -639,13 +639,14 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     int64_t limit = static_cast<int64_t>(device_optin_smem()) - static_smem;
     if (limit > kSmemBudget) limit = kSmemBudget;
     size_t smem = 0;
-    int cps = 1;
-    if (kCtasPerSm > 1) {
-        // Each CTA's share of the SM's shared memory, less the per-CTA reservation.
-        int64_t share = static_cast<int64_t>(device_sm_smem()) / kCtasPerSm - 1024 - static_smem;
+    // The most CTAs per SM (up to kCtasPerSm) whose share of the SM's shared
+    // memory, less the per-CTA reservation, holds a row buffer per warp.
+    int cps = kCtasPerSm;
+    for (; cps > 1; --cps) {
+        int64_t share = static_cast<int64_t>(device_sm_smem()) / cps - 1024 - static_smem;
         if (share > limit) share = limit;
         fused_plan(s, share, &a.nb, &a.ab_off, &smem);
-        if (a.nb >= 1) cps = kCtasPerSm;
+        if (a.nb >= 1) break;
     }
     if (cps == 1) fused_plan(s, limit, &a.nb, &a.ab_off, &smem);
     if (a.nb < 1) return cudaErrorInvalidConfiguration;
