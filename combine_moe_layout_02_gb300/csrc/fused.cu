@@ -167,7 +167,9 @@ __device__ bool phase_counts(const FusedArgs& a, int32_t* region) {
     const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
     const int W = (P + 31) / 32;
     bool bad = false;
-    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * kWarps + warp; ch < a.PC; ch += total_warps) {
+    // Channels are dealt warp-major (warp w of every CTA before warp w + 1), so
+    // a few hundred of them spread over all SMs rather than the first CTAs'.
+    for (int64_t ch = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x; ch < a.PC; ch += total_warps) {
         const uint32_t s32 = static_cast<uint32_t>(ch) / static_cast<uint32_t>(a.C);
         const int64_t s = s32, c = ch - static_cast<int64_t>(s32) * a.C;
         int64_t b, e;
@@ -310,7 +312,7 @@ __device__ void phase_tables(const FusedArgs& a, int32_t* region) {
     int32_t* colx = region + warp * colx_words(a.PC);
     const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
     const int64_t tasks = static_cast<int64_t>(a.P) + a.E;
-    for (int64_t task = static_cast<int64_t>(blockIdx.x) * kWarps + warp; task < tasks; task += total_warps) {
+    for (int64_t task = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x; task < tasks; task += total_warps) {
         if (task < a.P)
             scan_rank_column(a, static_cast<int>(task), colx, lane);
         else
@@ -379,7 +381,7 @@ __device__ void phase_payload(const FusedArgs& a, Ring& ring, int64_t* prb) {
     const DispatchArgs& d = a.d;
     const int64_t n_local = ring.n_local;
     const int64_t TW = static_cast<int64_t>(gridDim.x) * kWarps;
-    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    const int64_t gwarp = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x;  // warp-major, as in phase A
     const uint32_t RB = static_cast<uint32_t>(a.H) * 2u;
 
     Route cur, nxt;
