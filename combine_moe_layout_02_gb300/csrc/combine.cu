@@ -12,7 +12,10 @@
 // separately (__fmul_rn / __fadd_rn), ranks are visited in ascending order,
 // so the result is the same bit pattern on every run.
 //
-// Design (sm_103a): persistent grid, one warp per token, no block barriers.
+// Design (sm_103a): persistent grid, no block barriers. The unit of work is a
+// (token, column half): a warp takes units u, u + warps, ... so the last round
+// of a launch leaves few warps idle (whole tokens left about half the warps
+// idle for the last of ~14 rounds at 32768 tokens).
 //  * The warp compacts the token's send_head row into (row address, weight)
 //    pairs in ascending rank order (ballot, then the r-th set bit's lane hands
 //    its pair to lane r), then broadcasts the pairs to every lane once.
@@ -20,8 +23,8 @@
 //    chunks from all of the token's rows before reducing any of them, so up to
 //    kUnroll x MAXR x 16 bytes per lane are in flight, and stores 16 bytes of
 //    out per chunk.
-//  * The routing words of the warp's next token (send_head row, Top-K ids and
-//    weights) are loaded before the current token's rows, so their latency
+//  * The routing words of the warp's next unit (send_head row, Top-K ids and
+//    weights) are loaded before the current unit's rows, so their latency
 //    overlaps the payload traffic.
 #include <cuda_bf16.h>
 
@@ -33,12 +36,17 @@
 #ifndef MOE_COMBINE_UNROLL
 #define MOE_COMBINE_UNROLL 2
 #endif
+// Column parts per token: the unit of work a warp takes is (token, part).
+#ifndef MOE_COMBINE_SPLIT
+#define MOE_COMBINE_SPLIT 2
+#endif
 
 namespace moe {
 namespace {
 
 constexpr int kCombineThreads = MOE_COMBINE_THREADS;
 constexpr int kUnroll = MOE_COMBINE_UNROLL;
+constexpr int kSplit = MOE_COMBINE_SPLIT;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -84,10 +92,15 @@ __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_k
     __syncthreads();
     const int nchunks = a.H / 8;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5);
-    TokenRoute cur = load_route<EXPERT>(a, g, lane);
-    for (; g < a.S; g += warps_total) {
-        const TokenRoute nxt = load_route<EXPERT>(a, g + warps_total, lane);
+    const int64_t units = a.S * kSplit;
+    int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5);
+    TokenRoute cur = load_route<EXPERT>(a, u / kSplit, lane);
+    for (; u < units; u += warps_total) {
+        const int64_t g = u / kSplit;
+        const int part = static_cast<int>(u - g * kSplit);
+        const int cb = static_cast<int>((static_cast<int64_t>(nchunks) * part) / kSplit);
+        const int ce = static_cast<int>((static_cast<int64_t>(nchunks) * (part + 1)) / kSplit);
+        const TokenRoute nxt = load_route<EXPERT>(a, (u + warps_total) / kSplit, lane);
         const int32_t dk = (cur.idx >= 0 && cur.idx < a.E) ? cur.idx / a.epr : -1;
         // Compaction: lane r ends up holding the r-th valid rank's row and weight.
         uint64_t my_row = 0;
@@ -151,31 +164,31 @@ __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_k
             coef[r] = __shfl_sync(0xffffffffu, my_coef, r);
         }
         uint16_t* out = a.out + g * a.H;
-        for (int j0 = lane; j0 < nchunks; j0 += 32 * kUnroll) {
+        for (int j0 = cb + lane; j0 < ce; j0 += 32 * kUnroll) {
             uint4 v[kUnroll][MAXR];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int j = j0 + 32 * u;
+            for (int q = 0; q < kUnroll; ++q) {
+                const int j = j0 + 32 * q;
 #pragma unroll
                 for (int r = 0; r < MAXR; ++r)
-                    if (r < n && j < nchunks) v[u][r] = ld_stream_u4(rows[r] + static_cast<size_t>(j) * 16);
+                    if (r < n && j < ce) v[q][r] = ld_stream_u4(rows[r] + static_cast<size_t>(j) * 16);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int j = j0 + 32 * u;
-                if (j < nchunks) {
+            for (int q = 0; q < kUnroll; ++q) {
+                const int j = j0 + 32 * q;
+                if (j < ce) {
                     float acc[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
                     for (int r = 0; r < MAXR; ++r) {
                         if (r < n) {
-                            const uint32_t w4[4] = {v[u][r].x, v[u][r].y, v[u][r].z, v[u][r].w};
+                            const uint32_t w4[4] = {v[q][r].x, v[q][r].y, v[q][r].z, v[q][r].w};
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(coef[r], bf16_lo(w4[q])));
-                                acc[2 * q + 1] =
-                                    __fadd_rn(acc[2 * q + 1], __fmul_rn(coef[r], bf16_hi(w4[q])));
+                            for (int h = 0; h < 4; ++h) {
+                                acc[2 * h] = __fadd_rn(acc[2 * h], __fmul_rn(coef[r], bf16_lo(w4[h])));
+                                acc[2 * h + 1] =
+                                    __fadd_rn(acc[2 * h + 1], __fmul_rn(coef[r], bf16_hi(w4[h])));
                             }
                         }
                     }
@@ -202,7 +215,7 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     if (per_sm < 1) per_sm = 1;
     const int64_t warps_per_block = kCombineThreads / 32;
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
-    const int64_t needed = ceil_div(a.S, warps_per_block);
+    const int64_t needed = ceil_div(a.S * kSplit, warps_per_block);
     if (grid > needed) grid = needed;
     return launch_pdl(combine_kernel<MAXR, EXPERT>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a);
 }
