@@ -13,9 +13,11 @@
 // so the result is the same bit pattern on every run.
 //
 // Design (sm_103a): persistent grid, no block barriers. The unit of work is a
-// (token, column half): a warp takes units u, u + warps, ... so the last round
-// of a launch leaves few warps idle (whole tokens left about half the warps
-// idle for the last of ~14 rounds at 32768 tokens).
+// token, or a (token, column half) when the tokens would take at least
+// MOE_COMBINE_SPLIT_ROUNDS rounds of the launch's warps: a warp takes units u,
+// u + warps, ..., and halves keep the last round nearly full (whole tokens
+// left about half the warps idle for the last of ~14 rounds at 32768 tokens;
+// with only a few rounds the second compaction per token costs more).
 //  * The warp compacts the token's send_head row into (row address, weight)
 //    pairs in ascending rank order (ballot, then the r-th set bit's lane hands
 //    its pair to lane r), then broadcasts the pairs to every lane once.
@@ -36,9 +38,9 @@
 #ifndef MOE_COMBINE_UNROLL
 #define MOE_COMBINE_UNROLL 2
 #endif
-// Column parts per token: the unit of work a warp takes is (token, part).
-#ifndef MOE_COMBINE_SPLIT
-#define MOE_COMBINE_SPLIT 2
+// Whole-token rounds per warp from which tokens are split into column halves.
+#ifndef MOE_COMBINE_SPLIT_ROUNDS
+#define MOE_COMBINE_SPLIT_ROUNDS 8
 #endif
 
 namespace moe {
@@ -46,7 +48,7 @@ namespace {
 
 constexpr int kCombineThreads = MOE_COMBINE_THREADS;
 constexpr int kUnroll = MOE_COMBINE_UNROLL;
-constexpr int kSplit = MOE_COMBINE_SPLIT;
+constexpr int64_t kSplitRounds = MOE_COMBINE_SPLIT_ROUNDS;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -84,7 +86,8 @@ __device__ __forceinline__ TokenRoute load_route(const CombineArgs& a, int64_t g
 }
 
 template <int MAXR, bool EXPERT>
-__global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2)
+combine_kernel(const CombineArgs a, int split_shift) {
     pdl_wait_then_release();
     extern __shared__ __align__(16) int64_t prb[];  // [P+1]
     const int tid = threadIdx.x, lane = tid & 31;
@@ -92,15 +95,15 @@ __global__ void __launch_bounds__(kCombineThreads, MAXR >= 16 ? 1 : 2) combine_k
     __syncthreads();
     const int nchunks = a.H / 8;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t units = a.S * kSplit;
+    const int64_t units = a.S << split_shift;
     int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5);
-    TokenRoute cur = load_route<EXPERT>(a, u / kSplit, lane);
+    TokenRoute cur = load_route<EXPERT>(a, u >> split_shift, lane);
     for (; u < units; u += warps_total) {
-        const int64_t g = u / kSplit;
-        const int part = static_cast<int>(u - g * kSplit);
-        const int cb = static_cast<int>((static_cast<int64_t>(nchunks) * part) / kSplit);
-        const int ce = static_cast<int>((static_cast<int64_t>(nchunks) * (part + 1)) / kSplit);
-        const TokenRoute nxt = load_route<EXPERT>(a, (u + warps_total) / kSplit, lane);
+        const int64_t g = u >> split_shift;
+        const int part = static_cast<int>(u - (g << split_shift));
+        const int cb = static_cast<int>((static_cast<int64_t>(nchunks) * part) >> split_shift);
+        const int ce = static_cast<int>((static_cast<int64_t>(nchunks) * (part + 1)) >> split_shift);
+        const TokenRoute nxt = load_route<EXPERT>(a, (u + warps_total) >> split_shift, lane);
         const int32_t dk = (cur.idx >= 0 && cur.idx < a.E) ? cur.idx / a.epr : -1;
         // Compaction: lane r ends up holding the r-th valid rank's row and weight.
         uint64_t my_row = 0;
@@ -214,10 +217,14 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t warps_per_block = kCombineThreads / 32;
-    int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
-    const int64_t needed = ceil_div(a.S * kSplit, warps_per_block);
+    const int64_t full_grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+    // Column halves only when whole tokens would take many rounds of the warps.
+    const int split_shift = a.S >= kSplitRounds * full_grid * warps_per_block ? 1 : 0;
+    int64_t grid = full_grid;
+    const int64_t needed = ceil_div(a.S << split_shift, warps_per_block);
     if (grid > needed) grid = needed;
-    return launch_pdl(combine_kernel<MAXR, EXPERT>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a);
+    return launch_pdl(combine_kernel<MAXR, EXPERT>, static_cast<unsigned>(grid), kCombineThreads, smem, stream, a,
+                      split_shift);
 }
 
 template <bool EXPERT>
