@@ -179,6 +179,13 @@ def test_invalid_arguments_rejected_on_host():
 
 # ---- full sizes, launch configuration of the benchmark: sampled outputs ----
 
+def test_combine_column_halves_with_odd_chunk_count():
+    """Enough tokens that combine deals (token, column half) units at any
+    occupancy; H = 72 is 9 chunks of 8, so the halves are 4 and 5 chunks."""
+    w = inputs.make(4, 16, 50000, 72, 2, seed=21, mask_frac=0.05)
+    _check_all(w, sample=2000)
+
+
 @pytest.mark.parametrize("name,quant,y_mode", [
     ("p8_e256_t4096_h7168", 0, "identity"),
     ("p8_e256_t4096_h7168_int8", 1, "int8expert"),
