@@ -283,6 +283,33 @@ def test_int8_exact_ties_take_the_division_path():
     _check_all(w, quant=1, y_mode="int8expert")
 
 
+def test_int8_quantisation_over_every_bf16_value():
+    """For 65 amax values spread over the whole bf16 range (denormal to the
+    largest finite), rows that hold amax and every bf16 value of magnitude at
+    most amax: each int8 byte and scale equals the oracle's (IEEE division,
+    round half to even) -- the ties that bf16 ratios hit included."""
+    H = 16384
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    rows = []
+    for b in [(e << 7) | m for e in range(0, 255, 12) for m in (0, 0x2A, 0x7F)]:
+        if b == 0:
+            continue
+        amax = (np.array([b], np.uint32) << 16).view(np.float32)[0]
+        sel = bits[finite & (np.abs(vals) <= amax)].astype(np.uint16)
+        for r0 in range(0, sel.shape[0], H - 1):
+            row = np.zeros(H, np.uint16)
+            row[0] = b
+            chunk = sel[r0:r0 + H - 1]
+            row[1:1 + chunk.shape[0]] = chunk
+            rows.append(row)
+    x = np.stack(rows)
+    w = inputs.make(1, 1, x.shape[0], H, 1, seed=41, quant=1)
+    w.x_bits = x
+    _check_all(w, quant=1, y_mode="random")
+
+
 @pytest.mark.parametrize("H", [16384, 1024])
 def test_int8_ring_depths(H):
     """int8 dispatch with 32 KB rows (ring of one slot per consumer warp) and
