@@ -40,8 +40,9 @@ def run_gpu(w, quant=0, weights=True, arena_rows=None, part_row_base=None, y_mod
 
     part_row_base (host int64 [P+1]) replaces notify's packed bases before
     dispatch (fixed-capacity partitions). y_mode: "identity" (combine reads the
-    dispatch arena), "int8expert" (the stand-in expert above), or "random"
-    (fresh bf16 rows in a compact [rows, H] tensor).
+    dispatch arena), "int8expert" (the stand-in expert above), "random"
+    (fresh bf16 rows in a compact [rows, H] tensor), "allbf16" (every finite
+    bf16 value, in a seeded order) or "fill:0x...." (one bf16 bit pattern).
     """
     import torch
 
@@ -78,6 +79,19 @@ def run_gpu(w, quant=0, weights=True, arena_rows=None, part_row_base=None, y_mod
         elif y_mode == "random":
             g = torch.Generator(device="cpu").manual_seed(1234)
             y = torch.randn((buf.arena_rows, w.H), generator=g).to(torch.bfloat16).view(torch.int16).to(dev)
+            y_stride, y_rows = 2 * w.H, buf.arena_rows
+        elif y_mode.startswith("fill:"):
+            # every y element the given bf16 bit pattern, e.g. "fill:0x7f7f"
+            pattern = np.int16(np.uint16(int(y_mode[5:], 16)).view(np.int16))
+            y = torch.full((buf.arena_rows, w.H), int(pattern), dtype=torch.int16, device=dev)
+            y_stride, y_rows = 2 * w.H, buf.arena_rows
+        elif y_mode == "allbf16":
+            # every finite bf16 value (denormals, zeros of both signs, the
+            # largest magnitudes), repeated in a seeded order
+            bits = np.arange(1 << 16, dtype=np.uint32)
+            finite = bits[(bits & 0x7F80) != 0x7F80].astype(np.uint16)
+            order = np.random.default_rng(77).permutation(np.resize(finite, buf.arena_rows * w.H))
+            y = torch.from_numpy(order.reshape(buf.arena_rows, w.H).view(np.int16)).to(dev)
             y_stride, y_rows = 2 * w.H, buf.arena_rows
         else:
             raise ValueError(y_mode)

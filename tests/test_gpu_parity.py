@@ -179,6 +179,27 @@ def test_invalid_arguments_rejected_on_host():
 
 # ---- full sizes, launch configuration of the benchmark: sampled outputs ----
 
+@pytest.mark.parametrize("weights", [True, False])
+def test_combine_over_every_finite_bf16_value(weights):
+    """Expert outputs drawn from every finite bf16 value (denormals, both
+    zeros, the largest magnitudes, so sums can overflow to infinity): combine
+    equals the oracle bit for bit, with softmax and with unit weights."""
+    w = inputs.make(8, 64, 512, 1024, 8, seed=51, mask_frac=0.05)
+    _check_all(w, weights=weights, y_mode="allbf16")
+
+
+@pytest.mark.parametrize("pattern,weights", [("0x7f7f", False), ("0xff7f", False), ("0x0001", True),
+                                             ("0x8001", True)])
+def test_combine_overflow_and_denormal_sums(pattern, weights):
+    """Every expert output the largest finite bf16 (unit weights: a token on two
+    or more ranks sums to infinity) or the smallest denormal (softmax weights:
+    denormal products and sums), either sign: combine equals the oracle."""
+    w = inputs.make(8, 64, 64, 256, 8, seed=53, mask_frac=0.05)
+    gpu, _, _ = _check_all(w, weights=weights, y_mode="fill:" + pattern)
+    if pattern in ("0x7f7f", "0xff7f"):
+        assert ((gpu["out"] & 0x7FFF) == 0x7F80).any()  # some sums overflowed
+
+
 def test_combine_column_halves_with_odd_chunk_count():
     """Enough tokens that combine deals (token, column half) units at any
     occupancy; H = 72 is 9 chunks of 8, so the halves are 4 and 5 chunks."""
