@@ -180,7 +180,8 @@ moe_status moe_notify(const moe_shape* shape, const int32_t* num_tokens_per_rank
  *   quant = 0: the bf16 row x[g], bit for bit;
  *   quant = 1: q[h] = clamp(rint(f32(x[g][h]) / scale), -127, 127) as int8 and
  *              scale = amax / 127 (binary32, round to nearest even; amax = max|x[g]|;
- *              amax == 0 gives scale 0 and q 0);
+ *              amax == 0 gives scale 0 and q 0). Defined for finite x: a row with
+ *              an infinity or NaN gets unspecified codes and scale (no error);
  *   the triple (g / T, g % T, lowest k with topk_idx[g][k] / (E/P) == d).
  * Side arrays (each may be NULL), indexed by arena row:
  *   recv_src_idx      int32 [arena_rows]    g % T
