@@ -300,30 +300,52 @@ def host_info():
     return info
 
 
+def reference_tokens(args, budget_s: float = 120.0) -> int:
+    """Tokens per rank of the oracle arm's sample: the workload's own T when
+    the whole --warmup + --steps run fits the time budget on this host, else
+    the largest T that does (speed taken from one calibration pass)."""
+    from combine_moe_layout_02_gb300 import inputs
+
+    if args.ref_tokens:
+        return args.ref_tokens
+    full_T = inputs.WORKLOADS[args.workload]["T"]
+    T_cal = min(full_T, 64)
+    tps, _, _, _ = oracle_sample(args.workload, T_cal, 0.0, max_passes=1, layout=args.layout)
+    per_step = budget_s / (args.steps + args.warmup)
+    P = inputs.WORKLOADS[args.workload]["P"]
+    T = int(tps * per_step / P)
+    return max(1, min(full_T, T))
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
     from combine_moe_layout_02_gb300 import inputs
 
-    w = inputs.workload(args.workload, T=args.ref_tokens)
+    T_ref = reference_tokens(args)
+    w = inputs.workload(args.workload, T=T_ref)
     y_int8 = int8_stand_in(w, args.layout) if w.quant else None  # drawn once, untimed
     for _ in range(args.warmup):
-        oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w, layout=args.layout,
-                      y_int8=y_int8)
+        oracle_sample(args.workload, T_ref, 0.0, max_passes=1, workload=w, layout=args.layout, y_int8=y_int8)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, _, _, sample = oracle_sample(args.workload, args.ref_tokens, 0.0, max_passes=1, workload=w,
+        _, _, _, sample = oracle_sample(args.workload, T_ref, 0.0, max_passes=1, workload=w,
                                         layout=args.layout, y_int8=y_int8)
     elapsed = time.perf_counter() - t0
     value = w.S * args.steps / elapsed
     sample = sample.replace("1 pass(es)", f"{args.steps} timed steps of 1 pass")
+    full = inputs.WORKLOADS[args.workload]["T"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(w.quant),
         "data": "synthetic",
-        "config": dict(workload_config(args.workload, args.tokens_per_rank), layout=args.layout,
-                       fused=bool(args.fused), graph=bool(args.graph)),
+        # The config of what was timed: the workload at T_ref tokens per rank
+        # (the full workload when the run fits the time budget).
+        "config": dict(workload_config(args.workload, T_ref), layout=args.layout,
+                       fused=bool(args.fused), graph=bool(args.graph),
+                       sample=("full workload" if T_ref == full else
+                               f"T={T_ref} of the workload's {full} tokens per rank (time budget)")),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample, "GB_s": oracle_gbs(value), "host": host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -428,11 +450,17 @@ def run_ours(args, world, rank, local):
     R = int((buf.expert_part_base if expert else buf.part_row_base)[-1].item())
 
     # Working sets below twice the L2 would be served from L2 across steps:
-    # then a buffer larger than L2 is written before every timed step, outside
-    # that step's events.
+    # then a buffer of twice the L2 is READ before every timed step, outside
+    # that step's events. Reading (a sum over it) leaves L2 holding that
+    # buffer's clean lines, so the step neither finds its data in L2 nor pays
+    # for writing back the flush's own dirty lines.
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES)
     footprint = 2 * x.numel() + R * buf.stride + 2 * out.numel() + (2 * y_out.numel() if y_out is not None else 0)
-    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if footprint < 2 * l2 else None
+    flush_buf = torch.ones(2 * l2 // 8, dtype=torch.int64, device=dev) if footprint < 2 * l2 else None
+    flush_sink = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def flush():
+        torch.sum(flush_buf, dim=0, keepdim=True, out=flush_sink)
 
     def run_steps(n, fn):
         """Device seconds of n calls of fn (summed per call when flushing)."""
@@ -446,7 +474,7 @@ def run_ours(args, world, rank, local):
             return a.elapsed_time(b) / 1e3
         pairs = []
         for i in range(n):
-            flush_buf.fill_(i & 0xFF)
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -492,13 +520,37 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     for i, e in enumerate(evs):
         if flush_buf is not None:
-            flush_buf.fill_(i & 0xFF)
+            flush()
         step(e)
     torch.cuda.synchronize(dev)
-    t_front = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_front_ev = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     t_disp = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     t_comb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
     med = [statistics.median(e[a].elapsed_time(e[a + 1]) for e in evs) * 1e3 for a in range(3)]
+
+    # --- what layout + notify cost inside a step --------------------------
+    # An event recorded between two kernels ends the programmatic overlap of
+    # the second with the first, so the bracketed time above also holds the
+    # launch gaps the events create. The cost a step pays is the difference
+    # between whole steps and steps without layout and notify (dispatch and
+    # combine reuse the handle of the last notify), timed the same way.
+    def step_without_front(st=None):
+        st = stream if st is None else st
+        if fused:
+            buf.dispatch_fused(x, idx, wts, st)
+        elif expert:
+            buf.dispatch_expert(x, idx, wts, st)
+        else:
+            buf.dispatch(x, idx, wts, st)
+        if expert:
+            buf.combine_expert(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=st)
+        else:
+            buf.combine(out, idx, wts, y=y_out, y_row_stride=y_stride, stream=st)
+
+    n_front = max(args.steps, 20)
+    t_whole = run_steps(n_front, step)
+    t_rest = run_steps(n_front, step_without_front)
+    t_front = max(0.0, (t_whole - t_rest) / n_front)
     peak, peak_kind = measured_peaks()
     if expert:
         db = dispatch_expert_bytes(w.S, w.K, w.H, R, w.quant)
@@ -543,7 +595,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, passes, secs, sample = oracle_sample(args.workload, args.ref_tokens, args.cpu_seconds,
+        tps, passes, secs, sample = oracle_sample(args.workload, args.cpu_tokens, args.cpu_seconds,
                                                   layout=args.layout)
         cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
                "GB_s": oracle_gbs(tps), "host": host_info()}
@@ -559,9 +611,11 @@ def run_ours(args, world, rank, local):
                        l2=("no flush: working set (x, receive arena, out) of "
                            f"{footprint / 1e6:.0f} MB is larger than twice the {l2 / 1e6:.0f} MB L2"
                            if flush_buf is None else
-                           f"flushed: a {2 * l2 / 1e6:.0f} MB buffer is written before every timed step, "
+                           f"flushed: a {2 * l2 / 1e6:.0f} MB buffer is read before every timed step, "
                            f"outside its events (working set {footprint / 1e6:.0f} MB)")),
-        "gpu_launches": (3 if args.fused else (9 if expert else 6)) * args.steps,
+        # per step: layout (+ its error fold), notify, [notify_expert: 3,] dispatch, combine;
+        # the fused path: prep + fused launch, combine
+        "gpu_launches": (3 if args.fused else (8 if expert else 5)) * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "traffic": recorded_traffic(traffic_key(args.workload, args.tokens_per_rank, args.layout),
@@ -569,6 +623,9 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes": db if dominant == "dispatch" else cb},
         "stages": {
             "layout_notify_us": 1e6 * t_front,
+            "layout_notify_method": ("whole steps minus steps without layout and notify (the cost inside a "
+                                     "step); layout_notify_event_us brackets the two calls with events"),
+            "layout_notify_event_us": 1e6 * t_front_ev,
             "dispatch": {"us": 1e6 * t_disp, "GB_s": disp_gbs, "frac_of_peak": disp_gbs / peak,
                          "frac_of_8TBs": disp_gbs / 8000.0, "tokens_per_s": w.S / t_disp,
                          "bytes": db},
@@ -603,8 +660,11 @@ def main(argv=None):
                     help="layout + notify + dispatch as one cooperative launch (small shapes)")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="override T (a smaller case of the same workload, e.g. for profiling)")
-    ap.add_argument("--ref-tokens", type=int, default=512,
-                    help="tokens per rank of the oracle's bounded sample")
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="tokens per rank of the oracle arm's sample (default: the workload's own T when the "
+                         "run fits about two minutes, else the largest T that does)")
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="tokens per rank of the GPU arm's cpu_baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

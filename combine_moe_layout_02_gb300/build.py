@@ -2,6 +2,14 @@
 
 Each translation unit is compiled in parallel into ``_build/``; the shared
 library is linked next to this file, where the binding loads it from.
+
+Variants (``python -m combine_moe_layout_02_gb300.build --variant NAME``) are
+the same sources compiled with extra defines into ``libmoe_NAME.so``; the
+binding loads one when ``MOE_LIBRARY=NAME`` is set:
+  match_hist   layout's histograms in the atomics-free grouped form
+               (-DMOE_LAYOUT_MATCH_HIST) instead of shared-memory atomics
+  profile      kernels record per-CTA phase times into a device array
+               attached with moe_profile_attach (-DMOE_PROFILE)
 """
 
 from __future__ import annotations
@@ -21,6 +29,11 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "layout.cu", "notify.cu", "dispatch.cu", "combine.cu", "layout_static.cu", "pad.cu", "expert.cu", "fused.cu", "run.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+VARIANTS = {"match_hist": ["-DMOE_LAYOUT_MATCH_HIST"], "profile": ["-DMOE_PROFILE"]}
+
+
+def lib_path(variant: str | None = None) -> str:
+    return LIB if not variant else os.path.join(HERE, f"libmoe_{variant}.so")
 
 
 def nvcc() -> str:
@@ -42,10 +55,13 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, variant: str | None = None) -> str:
+    defines = VARIANTS[variant] if variant else []
+    out_dir = os.path.join(BUILD, variant) if variant else BUILD
+    lib = lib_path(variant)
+    os.makedirs(out_dir, exist_ok=True)
     # Objects built on another host architecture are never reused.
-    stamp = os.path.join(BUILD, "HOST")
+    stamp = os.path.join(out_dir, "HOST")
     host = platform.machine()
     if not os.path.exists(stamp) or open(stamp).read().strip() != host:
         force = True
@@ -55,10 +71,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     objs = []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or ptxas_info or _stale(obj, [path, *headers]):
-            extra = ["-Xptxas", "-v"] if ptxas_info else []
+            extra = (["-Xptxas", "-v"] if ptxas_info else []) + defines
             jobs.append([cc, *_flags(extra), "-c", path, "-o", obj])
 
     def run(cmd):
@@ -74,17 +90,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
     with open(stamp, "w") as f:
         f.write(host + "\n")
-    if force or jobs or _stale(LIB, objs) or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs) or not os.path.exists(lib):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    var = sys.argv[sys.argv.index("--variant") + 1] if "--variant" in sys.argv else None
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv, variant=var))

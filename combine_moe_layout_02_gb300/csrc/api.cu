@@ -99,6 +99,60 @@ cudaError_t prepare_kernel(const void* fn, size_t smem, int threads, int* per_sm
     return cudaSuccess;
 }
 
+namespace {
+
+struct ClusterEntry {
+    const void* fn;
+    int dev, want, threads, result;
+    size_t smem;
+};
+ClusterEntry g_clusters[256];
+int g_nclusters = 0;
+
+}  // namespace
+
+int cluster_size_for(const void* fn, int want_in, int threads, size_t smem) {
+    int want = want_in;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    {
+        std::lock_guard<std::mutex> lock(g_kernel_mu);
+        for (int i = 0; i < g_nclusters; ++i) {
+            const ClusterEntry& c = g_clusters[i];
+            if (c.fn == fn && c.dev == dev && c.want == want_in && c.threads == threads && c.smem == smem)
+                return c.result;
+        }
+    }
+    int result = -1;
+    // Clusters above the portable 8 CTAs must be allowed per kernel.
+    if (want > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        want = 8;
+    }
+    for (int c = want; c >= 1; c /= 2) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(c));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) {
+            result = c;
+            break;
+        }
+        cudaGetLastError();  // clear a refusal of this size before trying the next
+    }
+    std::lock_guard<std::mutex> lock(g_kernel_mu);
+    if (result > 0 && g_nclusters < 256) g_clusters[g_nclusters++] = ClusterEntry{fn, dev, want_in, threads, result, smem};
+    return result;
+}
+
 int kernel_static_smem(const void* fn) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -460,6 +514,18 @@ moe_status moe_combine_expert(const moe_shape* shape, const void* y, int64_t y_r
     a.slot_row = slot_row;
     return from_cuda(launch_combine_expert(s, a, static_cast<cudaStream_t>(stream)));
 }
+
+#ifdef MOE_PROFILE
+moe_status moe_profile_attach(void* slots, int64_t bytes) {
+    const int64_t need = static_cast<int64_t>(kProfKernels) * kProfCtas * kProfPhases * 8;
+    if (slots != nullptr && (bytes < need || !aligned(slots, 16))) return MOE_ERR_INVALID_ARG;
+    cudaError_t (*attach[])(void*) = {prof_attach_layout, prof_attach_notify, prof_attach_dispatch,
+                                      prof_attach_combine, prof_attach_fused, prof_attach_expert};
+    for (auto f : attach)
+        if (f(slots) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+#endif
 
 moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_tokens,
                               const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,

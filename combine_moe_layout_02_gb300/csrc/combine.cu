@@ -247,4 +247,6 @@ cudaError_t launch_combine_expert(const moe_shape& s, CombineArgs a, cudaStream_
     return launch_combine_mode<true>(a, s.K, stream);  // one row per slot
 }
 
+MOE_PROFILE_UNIT(combine)
+
 }  // namespace moe

@@ -575,4 +575,6 @@ cudaError_t launch_dispatch_expert(const moe_shape& s, DispatchArgs a, cudaStrea
     return launch_dispatch_mode<true>(s, a, stream);
 }
 
+MOE_PROFILE_UNIT(dispatch)
+
 }  // namespace moe

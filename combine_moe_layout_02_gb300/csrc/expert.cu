@@ -219,4 +219,6 @@ cudaError_t launch_notify_expert(const moe_shape& s, const int32_t* topk_idx, co
                       static_cast<int64_t>(s.S), p.chunks, topk_idx, static_cast<const int32_t*>(ebase), slot_row);
 }
 
+MOE_PROFILE_UNIT(expert)
+
 }  // namespace moe

@@ -696,4 +696,6 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     return cudaLaunchKernelEx(&cfg, fused_kernel, a);
 }
 
+MOE_PROFILE_UNIT(fused)
+
 }  // namespace moe

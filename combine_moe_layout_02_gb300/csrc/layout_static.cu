@@ -3,20 +3,23 @@
 // Some callers of this library cannot call cudaMalloc: code hosted inside an
 // engine that owns every byte of device memory and forbids allocation once it
 // has started, and latency-bound serving loops where an allocation would
-// synchronise the device. moe_layout needs a scratch buffer for its per-block
-// partial counts; this entry point takes it from a buffer compiled into the
-// library instead, so the caller passes only the inputs and outputs.
+// synchronise the device. moe_layout needs a scratch array (one out-of-range
+// flag per source rank, folded into the error word by its tail kernel); this
+// entry point takes it from a buffer compiled into the library instead, so
+// the caller passes only the inputs and outputs.
 //
 // The buffer is a file-scope __device__ array of MOE_LAYOUT_STATIC_SCRATCH_BYTES
-// bytes. Every GPU that loads the library holds it until the process exits.
-// Host code cannot use the array's name as a device address, so the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it; that first call should therefore come before
-// any stream capture. All calls share the one buffer and it keeps the last
-// call's contents: the layout kernels write every partial before they read it,
-// so nothing has to start at zero, but calls that overlap on the GPU (on two
-// streams, or from two threads) race on it. Nothing here calls cudaMalloc,
-// cudaFree or any routine that allocates.
+// bytes, enough for the largest accepted shape. Every GPU that loads the
+// library holds it until the process exits. Host code cannot use the array's
+// name as a device address, so the first call on each device looks the
+// address up with cudaGetSymbolAddress (with that device current) and keeps
+// it; that first call should therefore come before any stream capture, and
+// the kept address assumes the device's context is never reset. All calls
+// share the one buffer and it keeps the last call's contents: the layout
+// kernel writes every flag before the tail kernel reads it, so nothing has to
+// start at zero, but calls that overlap on the GPU (on two streams, or from
+// two threads) race on it. Nothing here calls cudaMalloc, cudaFree or any
+// routine that allocates.
 #include <mutex>
 
 #include "moe.h"
@@ -71,7 +74,7 @@ extern "C" moe_status moe_layout_static_scratch(const moe_shape* shape, const in
         (is_token_in_rank_bits && !aligned16(is_token_in_rank_bits)) ||
         (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
         return MOE_ERR_INVALID_ARG;
-    // The partials of this shape must fit in the built-in buffer.
+    // The flags of this shape must fit in the built-in buffer.
     if (layout_plan(s).scratch_bytes > static_cast<int64_t>(MOE_LAYOUT_STATIC_SCRATCH_BYTES))
         return MOE_ERR_UNSUPPORTED;
     void* scratch = nullptr;

@@ -143,15 +143,97 @@ __host__ __device__ __forceinline__ void split_range(int64_t n, int64_t b, int64
 }
 
 // ---------------------------------------------------------------------------
+// Device-side phase profile (profile builds only, -DMOE_PROFILE; the default
+// build compiles these macros to nothing). An instrumented kernel calls
+// MOE_PROF_BEGIN(kernel) once, MOE_STAMP(p) at the end of phase p and
+// MOE_PROF_END() before it returns. Thread 0 of CTA b keeps the stamps in
+// shared memory while the kernel runs (a global store would make the next
+// cluster barrier's release wait for it) and writes them at the end to row
+//   slots[(kernel * kProfCtas + b) * kProfPhases ...]
+// of the array attached with moe_profile_attach: slot 0 = %globaltimer (ns) at
+// MOE_PROF_BEGIN, slot p = clock64 cycles from MOE_PROF_BEGIN to the end of
+// phase p (0 if not reached). CTAs at or beyond kProfCtas record nothing.
+// Loop phases that repeat inside a CTA (the int8 consumer's per-token steps)
+// instead add their cycles into a slot (MOE_PROF_ADD), summed by the CTA's
+// first consumer warp.
+#ifdef MOE_PROFILE
+constexpr int kProfKernels = MOE_PROF_KERNELS;
+constexpr int kProfCtas = MOE_PROF_CTAS;
+constexpr int kProfPhases = MOE_PROF_PHASES;
+enum ProfKernel { kProfLayout = 0, kProfNotify = 1, kProfDispatch = 2, kProfDispatchInt8 = 3, kProfCombine = 4,
+                  kProfFused = 5, kProfNotifyExpert = 6 };
+// One copy per translation unit, set by that unit's prof_attach_* function.
+static __device__ unsigned long long* g_prof_slots;
+
+__device__ __forceinline__ unsigned long long prof_globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned long long* prof_row(int kernel) {
+    unsigned long long* p = g_prof_slots;
+    if (p == nullptr || blockIdx.x >= static_cast<unsigned>(kProfCtas)) return nullptr;
+    return p + (static_cast<size_t>(kernel) * kProfCtas + blockIdx.x) * kProfPhases;
+}
+#define MOE_PROF_BEGIN(kernel)                                                        \
+    __shared__ unsigned long long moe_prof_sm_[kProfPhases];                          \
+    unsigned long long* const moe_prof_row_ = ::moe::prof_row(kernel);                \
+    const long long moe_prof_c0_ = clock64();                                         \
+    if (threadIdx.x == 0) {                                                           \
+        moe_prof_sm_[0] = ::moe::prof_globaltimer();                                  \
+        for (int moe_i_ = 1; moe_i_ < kProfPhases; ++moe_i_) moe_prof_sm_[moe_i_] = 0; \
+    }
+#define MOE_STAMP(phase)                                                              \
+    do {                                                                              \
+        if (threadIdx.x == 0)                                                         \
+            moe_prof_sm_[(phase)] = static_cast<unsigned long long>(clock64() - moe_prof_c0_); \
+    } while (0)
+#define MOE_PROF_END()                                                                \
+    do {                                                                              \
+        if (moe_prof_row_ && threadIdx.x == 0)                                        \
+            for (int moe_i_ = 0; moe_i_ < kProfPhases; ++moe_i_) moe_prof_row_[moe_i_] = moe_prof_sm_[moe_i_]; \
+    } while (0)
+#define MOE_PROF_ADD(phase, cycles)                                                   \
+    do {                                                                              \
+        if (moe_prof_row_) moe_prof_row_[(phase)] += (cycles);                        \
+    } while (0)
+// Defines prof_attach_<unit>(), which points this unit's kernels at `slots`.
+#define MOE_PROFILE_UNIT(unit)                                                      \
+    cudaError_t prof_attach_##unit(void* slots) {                                  \
+        unsigned long long* p = static_cast<unsigned long long*>(slots);           \
+        return cudaMemcpyToSymbol(g_prof_slots, &p, sizeof(p));                    \
+    }
+cudaError_t prof_attach_layout(void*);
+cudaError_t prof_attach_notify(void*);
+cudaError_t prof_attach_dispatch(void*);
+cudaError_t prof_attach_combine(void*);
+cudaError_t prof_attach_fused(void*);
+cudaError_t prof_attach_expert(void*);
+#else
+#define MOE_PROF_BEGIN(kernel) \
+    do {                       \
+    } while (0)
+#define MOE_PROF_END() \
+    do {               \
+    } while (0)
+#define MOE_STAMP(phase) \
+    do {                 \
+    } while (0)
+#define MOE_PROF_ADD(phase, cycles) \
+    do {                            \
+    } while (0)
+#define MOE_PROFILE_UNIT(unit)
+#endif
+
+// ---------------------------------------------------------------------------
 // Launchers (defined in layout.cu / notify.cu / dispatch.cu / combine.cu).
 // Shapes are validated by the C-ABI layer before these run.
 
 struct LayoutPlan {
-    int threads;       // tokens per block (one per thread)
-    int64_t blocks_per_source;
-    int64_t part_stride;  // int32 entries per block partial: P + E + 1
+    int cluster;   // CTAs per source rank (before the residency check)
+    int threads;   // tokens per block pass (one per thread)
     size_t smem;
-    int64_t scratch_bytes;
+    int64_t scratch_bytes;  // one out-of-range flag per source rank
 };
 LayoutPlan layout_plan(const moe_shape& s);
 cudaError_t launch_layout(const moe_shape& s, const int32_t* topk_idx, int32_t* ntpr, int32_t* ntpe,
@@ -254,6 +336,79 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch_pdl for a kernel whose blocks form thread-block clusters of
+// `cluster` CTAs along x (grid a multiple of cluster).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                               unsigned cluster, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Largest cluster size c in {want, want/2, ..., 1} for which clusters of c
+// CTAs of `fn` (threads, smem) can be resident on the current device; cached
+// per (kernel, device, want, threads, smem).
+int cluster_size_for(const void* fn, int want, int threads, size_t smem);
+
+// ---------------------------------------------------------------------------
+// Thread-block cluster helpers (distributed shared memory).
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Index of this CTA's cluster along x (the grid is clusters of CTAs along x).
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Full cluster barrier: release this thread's prior memory operations
+// (shared and distributed shared) and acquire the other CTAs'.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Split form of the barrier: arrive now, wait later (the CTA's shared memory
+// must stay valid until every peer has passed its wait).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (a shared-memory location of this CTA) in the shared
+// memory of cluster CTA `rank`, as a shared::cluster address.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(p)), "r"(rank));
+    return out;
+}
+
+__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t addr) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 }  // namespace moe

@@ -10,85 +10,76 @@
 // rank is the c-th block of the balanced split of "HCCL Window 模式
 // (Non-SHMEM) 代码深度剖析", section 8.3.
 //
-// Two launches. Work is handed out per warp, so every block shape works:
-//  1. notify_count_kernel
-//     - channel part: per-rank token counts of each (source rank, channel)
-//       into scratch;
-//     - rank part: one warp per destination column scans num_tokens_per_rank
-//       down the source ranks (warp-shuffle scan with a carry) into
-//       rank_prefix_matrix and num_recv_tokens;
-//     - expert part: one warp per expert sums num_tokens_per_expert over
-//       source ranks and rounds up to expert_alignment.
-//  2. notify_head_kernel
-//     - channel part: channel prefixes from the scratch counts, then
-//       send_head for the channel's tokens;
-//     - tail part: one warp per rank scans its per-expert counts into
-//       recv_expert_offset; warp 0 scans the receive totals into the packed
-//       partition bases.
-// The channel part has two shapes:
-//   * token-major (P < 32 or P % 4 != 0): one block per channel, one thread
-//     per token; per rank a __ballot_sync, __popc of the lower lanes for the
-//     rank inside the warp, and a scan over the block's warps;
-//   * rank-major (P >= 32, P % 4 == 0): one warp per channel, each lane owns 4
-//     ranks and walks the channel's tokens in order with 4 running counters;
-//     a token's send_head row is one coalesced 16-byte store per lane.
+// The receive position of token g of source rank s on rank d unrolls to
+//   rank_prefix[s-1][d] + (tokens of s before g that are bound for d):
+// the channels only cut that running count into the matrices' segments. So
+// every output of a source rank follows from its own rows of
+// is_token_in_rank plus sums of num_tokens_per_rank / num_tokens_per_expert,
+// and one launch suffices: one thread-block cluster per source rank s, with
+// no synchronisation between clusters.
+//
+// Inside the cluster each warp takes a contiguous segment of s's tokens.
+// Lanes are laid out as (token, group of 4 ranks): for P/4 <= 32 groups a
+// token takes L = the next power of two >= P/4 lanes and a warp covers 32/L
+// tokens per step (16 at P = 8, 1 at P = 128); each lane loads the token's 4
+// flags of its group as one 32-bit word.
+//  1. Count: each warp counts its segment's tokens per rank.
+//  2. Block: per-warp counts become exclusive warp offsets and CTA totals;
+//     cluster barrier; each CTA adds the totals of the CTAs before it
+//     (distributed shared memory) -- the segment bases.
+//  3. Heads: each warp walks its segment again; the 4 flags of a lane are
+//     packed one per byte, so one shuffle scan over the token lanes gives
+//     the exclusive counts of 4 ranks at once. send_head rows are written
+//     as 16-byte stores; a token that starts a channel writes that
+//     channel's recv_channel_prefix_matrix entry and the previous channel's
+//     channel_prefix_matrix entry.
+// Beside the scan, the cluster adds up rank_prefix_matrix's column prefix
+// over the earlier source ranks (split over its CTAs), and cluster s sums the
+// per-expert counts of rank s (num_recv_tokens_per_expert, recv_expert_offset);
+// cluster P-1 also writes num_recv_tokens and the packed partition bases.
 // No atomics: every output is a fixed-order integer sum.
 #include "moe_device.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kMaxThreads = 256;
+constexpr int kNotifyThreads = 256;
+constexpr int kNotifyWarps = kNotifyThreads / 32;
+constexpr int kNotifyMaxCluster = 16;
 
-struct NotifyPlan {
-    bool rank_major;
-    int threads;             // block size
-    int wpb;                 // warps per block
-    int64_t chan_blocks;     // blocks of the channel part
-    int64_t rank_blocks;     // kernel 1: rank-prefix blocks
-    int64_t expert_blocks;   // kernel 1: expert-sum blocks
-    int64_t tail_blocks;     // kernel 2: offset / base blocks
+constexpr int kNotifyCache = 4;          // flag words a lane keeps in registers between the passes
+static_assert(kNotifyCache == 4, "the second pass selects among exactly four cached words");
+constexpr int kNotifyChanBuf = 4096;     // int32 entries of the channel-start buffer
+
+struct NotifySmem {
+    size_t wcnt, xc, xr, tmp_r, base, total, rprev, ecnt, nrt64, chv, bytes;
 };
 
-NotifyPlan notify_plan(const moe_shape& s) {
-    NotifyPlan p;
-    const int64_t T = s.S / s.P;
-    const int64_t chans = static_cast<int64_t>(s.P) * s.num_channels;
-    p.rank_major = s.P >= 32 && (s.P % 4) == 0;
-    if (p.rank_major) {
-        p.threads = kMaxThreads;
-    } else {
-        int64_t t = round_up(ceil_div(T, s.num_channels), 32);
-        p.threads = static_cast<int>(t < 32 ? 32 : (t > kMaxThreads ? kMaxThreads : t));
-    }
-    p.wpb = p.threads / 32;
-    p.chan_blocks = p.rank_major ? ceil_div(chans, p.wpb) : chans;
-    p.rank_blocks = ceil_div(s.P, p.wpb);
-    p.expert_blocks = ceil_div(s.E, p.wpb);
-    p.tail_blocks = ceil_div(s.P, p.wpb);
-    return p;
-}
-
-// For each rank d, ballot "token of this lane is bound for d" over the warp and
-// hand the ballot to f(d, ballot). Loads the token's row 4 bytes at a time
-// when P is a multiple of 4 (rows then start 4-byte aligned).
-template <typename F>
-__device__ __forceinline__ void for_each_rank_ballot(const uint8_t* row, bool active, int P, F&& f) {
-    if ((P & 3) == 0) {
-        for (int d4 = 0; d4 < P; d4 += 4) {
-            const uint32_t w4 = active ? __ldg(reinterpret_cast<const uint32_t*>(row + d4)) : 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t bal = __ballot_sync(0xffffffffu, ((w4 >> (8 * j)) & 0xffu) != 0u);
-                f(d4 + j, bal);
-            }
-        }
-    } else {
-        for (int d = 0; d < P; ++d) {
-            const uint32_t bal = __ballot_sync(0xffffffffu, active && __ldg(row + d) != 0);
-            f(d, bal);
-        }
-    }
+// Shared memory (int32 unless noted): wcnt [warps][P]; xc, xr [cs][P] (the
+// cluster CTAs' totals and rank-prefix partials; this CTA's own row is the
+// one peers read); tmp_r [threads] int4; base [P];
+// total [P]; rprev [P]; ecnt [E/P]; nrt64 int64 [P]; chv [channels starting
+// in this CTA's tokens][P] when that fits kNotifyChanBuf.
+__host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs) {
+    NotifySmem m;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += (bytes + 15) / 16 * 16;
+        return at;
+    };
+    m.wcnt = take(static_cast<size_t>(kNotifyWarps) * P * 4);
+    m.xc = take(static_cast<size_t>(cs) * P * 4);
+    m.xr = take(static_cast<size_t>(cs) * P * 4);
+    m.tmp_r = take(kNotifyThreads * 16);
+    m.base = take(static_cast<size_t>(P) * 4);
+    m.total = take(static_cast<size_t>(P) * 4);
+    m.rprev = take(static_cast<size_t>(P) * 4);
+    m.ecnt = take(static_cast<size_t>(E / P) * 4);
+    m.nrt64 = take(static_cast<size_t>(P) * 8);
+    m.chv = take(kNotifyChanBuf * 4);
+    m.bytes = o;
+    return m;
 }
 
 template <typename V>
@@ -101,276 +92,486 @@ __device__ __forceinline__ V warp_inclusive_scan(V v, int lane) {
     return v;
 }
 
-__device__ __forceinline__ int flag(uint32_t w, int j) { return ((w >> (8 * j)) & 0xffu) != 0u; }
-
-// ---- kernel 1 -------------------------------------------------------------
-
-__global__ void __launch_bounds__(kMaxThreads)
-notify_count_kernel(int32_t P, int32_t E, int32_t C, int32_t A, int64_t T, bool rank_major,
-                    int64_t chan_blocks, int64_t rank_blocks, const int32_t* __restrict__ ntpr,
-                    const int32_t* __restrict__ ntpe, const uint8_t* __restrict__ itr,
-                    int32_t* __restrict__ rpm, int32_t* __restrict__ nrt, int32_t* __restrict__ nrtpe,
-                    int32_t* __restrict__ ccount) {
-    pdl_wait_then_release();
-    extern __shared__ __align__(16) int32_t wcnt[];  // token-major: [warps][P]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int wpb = nthreads >> 5;
-    const int64_t bid = blockIdx.x;
-
-    if (bid >= chan_blocks) {
-        if (bid < chan_blocks + rank_blocks) {
-            // Rank part: column d of num_tokens_per_rank, scanned over sources.
-            const int64_t gw = (bid - chan_blocks) * wpb + warp;
-            if (gw >= P) return;
-            const int d = static_cast<int>(gw);
-            int32_t carry = 0;
-            for (int s0 = 0; s0 < P; s0 += 32) {
-                const int s = s0 + lane;
-                const int32_t v = s < P ? __ldg(ntpr + static_cast<int64_t>(s) * P + d) : 0;
-                const int32_t incl = warp_inclusive_scan(v, lane);
-                if (s < P) rpm[static_cast<int64_t>(s) * P + d] = carry + incl;
-                carry += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) nrt[d] = carry;
-        } else {
-            // Expert part: receive count of expert e, summed over sources, aligned.
-            const int64_t gw = (bid - chan_blocks - rank_blocks) * wpb + warp;
-            if (gw >= E) return;
-            int64_t sum = 0;
-            for (int s = lane; s < P; s += 32) sum += __ldg(ntpe + static_cast<int64_t>(s) * E + gw);
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (lane == 0) nrtpe[gw] = static_cast<int32_t>(round_up(sum, A));
-        }
-        return;
-    }
-
-    if (rank_major) {
-        const int64_t ch = bid * wpb + warp;
-        if (ch >= static_cast<int64_t>(P) * C) return;
-        const int64_t s = ch / C, c = ch % C;
-        int64_t b, e;
-        split_range(T, C, c, &b, &e);
-        for (int d0 = 0; d0 < P; d0 += 128) {
-            const int d = d0 + 4 * lane;
-            if (d >= P) continue;
-            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-#pragma unroll 8
-            for (int64_t t = b; t < e; ++t) {
-                const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + (s * T + t) * P + d));
-                c0 += flag(w, 0);
-                c1 += flag(w, 1);
-                c2 += flag(w, 2);
-                c3 += flag(w, 3);
-            }
-            *reinterpret_cast<int4*>(ccount + ch * P + d) = make_int4(c0, c1, c2, c3);
-        }
-        return;
-    }
-
-    // Token-major channel counts.
-    const int64_t s = bid / C, c = bid % C;
-    int64_t b, e;
-    split_range(T, C, c, &b, &e);
-    for (int i = tid; i < wpb * P; i += nthreads) wcnt[i] = 0;
-    __syncthreads();
-    int32_t* mine = wcnt + warp * P;
-    for (int64_t t0 = b; t0 < e; t0 += nthreads) {
-        const int64_t t = t0 + tid;
-        const bool active = t < e;
-        const uint8_t* row = itr + (s * T + (active ? t : b)) * P;
-        for_each_rank_ballot(row, active, P, [&](int d, uint32_t bal) {
-            if (lane == (d & 31)) mine[d] += __popc(bal);
-        });
-    }
-    __syncthreads();
-    for (int d = tid; d < P; d += nthreads) {
-        int32_t sum = 0;
-        for (int w = 0; w < wpb; ++w) sum += wcnt[w * P + d];
-        ccount[bid * P + d] = sum;
-    }
+// Each byte of w that is nonzero becomes 1, the others 0.
+__device__ __forceinline__ uint32_t nz_bytes(uint32_t w) {
+    uint32_t t = w | (w >> 4);
+    t |= t >> 2;
+    t |= t >> 1;
+    return t & 0x01010101u;
 }
 
-// ---- kernel 2 -------------------------------------------------------------
+__device__ __forceinline__ int byte_of(uint32_t w, int j) { return static_cast<int>((w >> (8 * j)) & 0xffu); }
 
-__global__ void __launch_bounds__(kMaxThreads)
-notify_head_kernel(int32_t P, int32_t E, int32_t C, int64_t T, bool rank_major, int64_t chan_blocks,
-                   const uint8_t* __restrict__ itr, const int32_t* __restrict__ rpm,
-                   const int32_t* __restrict__ nrt, const int32_t* __restrict__ nrtpe,
-                   const int32_t* __restrict__ ccount, int32_t* __restrict__ cpm,
-                   int32_t* __restrict__ rcpm, int32_t* __restrict__ send_head,
-                   int32_t* __restrict__ reo, int64_t* __restrict__ part_row_base) {
+// Flags of ranks d..d+3 of row `row` (one per byte, 0/1); ranks >= P give 0.
+template <bool A4>
+__device__ __forceinline__ uint32_t load_flags(const uint8_t* row, int d, int P) {
+    if (A4) return nz_bytes(__ldg(reinterpret_cast<const uint32_t*>(row + d)));
+    uint32_t f = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (d + j < P && __ldg(row + d + j) != 0) f |= 1u << (8 * j);
+    return f;
+}
+
+// First token of channel c under the balanced split of T tokens over C
+// channels (q = T / C, rr = T % C; begin(C) = T).
+__device__ __forceinline__ int32_t channel_begin(int32_t c, int32_t q, int32_t rr) {
+    return c * q + min(c, rr);
+}
+
+// The first channel that starts at or after token t.
+__device__ __forceinline__ int32_t next_channel(int32_t t, int32_t q, int32_t rr) {
+    const int32_t bnd = rr * (q + 1);  // tokens in the rr longer channels
+    int32_t c = t < bnd ? t / (q + 1) : rr + (t - bnd) / q;
+    if (channel_begin(c, q, rr) < t) ++c;
+    return c;
+}
+
+// Shape constants of a launch, split on the host so that the kernel does no
+// integer division: T = tokens per source rank; cs = CTAs per cluster (a
+// power of two, 2^lcs); the warps' token segments are the balanced split of
+// T over cs * kNotifyWarps (wq, wr); the channels that of T over C (cq, cr);
+// each CTA sums a balanced share of rank s's E/P experts (eq, er).
+struct NotifyParams {
+    int32_t P, E, C, A, epr, T, cs, lcs;
+    int32_t wq, wr, cq, cr, eq, er;
+    const int32_t* ntpr;
+    const int32_t* ntpe;
+    const uint8_t* itr;
+    int32_t *rpm, *cpm, *rcpm, *nrt, *nrtpe, *reo, *send_head;
+    int64_t* part_row_base;
+};
+
+// Grid: P clusters of cs CTAs of kNotifyThreads threads; cluster s handles
+// source rank s.
+template <bool A4>
+__global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyParams a) {
     pdl_wait_then_release();
-    extern __shared__ __align__(16) int32_t sm[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int wpb = nthreads >> 5;
-    const int64_t bid = blockIdx.x;
+    MOE_PROF_BEGIN(kProfNotify);
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int32_t P = a.P, E = a.E, C = a.C, A = a.A;
+    const int32_t T = a.T;
+    const int32_t* __restrict__ ntpr = a.ntpr;
+    const int32_t* __restrict__ ntpe = a.ntpe;
+    const uint8_t* __restrict__ itr = a.itr;
+    int32_t* __restrict__ rpm = a.rpm;
+    int32_t* __restrict__ cpm = a.cpm;
+    int32_t* __restrict__ rcpm = a.rcpm;
+    int32_t* __restrict__ nrt = a.nrt;
+    int32_t* __restrict__ nrtpe = a.nrtpe;
+    int32_t* __restrict__ reo = a.reo;
+    int32_t* __restrict__ send_head = a.send_head;
+    int64_t* __restrict__ part_row_base = a.part_row_base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cs = a.cs;
+    const int r = static_cast<int>(cluster_ctarank());
+    const int32_t s = static_cast<int32_t>(cluster_id_x());
+    const NotifySmem M = notify_smem(P, E, cs);
+    int32_t* wcnt = reinterpret_cast<int32_t*>(smem + M.wcnt);
+    int32_t* xc = reinterpret_cast<int32_t*>(smem + M.xc);
+    int32_t* xr = reinterpret_cast<int32_t*>(smem + M.xr);
+    int4* tmp_r = reinterpret_cast<int4*>(smem + M.tmp_r);
+    int32_t* base = reinterpret_cast<int32_t*>(smem + M.base);
+    int32_t* total = reinterpret_cast<int32_t*>(smem + M.total);
+    int32_t* rprev = reinterpret_cast<int32_t*>(smem + M.rprev);
+    int32_t* ecnt = reinterpret_cast<int32_t*>(smem + M.ecnt);
+    int64_t* nrt64 = reinterpret_cast<int64_t*>(smem + M.nrt64);
+    int32_t* chv = reinterpret_cast<int32_t*>(smem + M.chv);
+    int32_t* ctot = xc + r * P;   // this CTA's totals (read by the peers)
+    int32_t* rpart = xr + r * P;  // this CTA's rank-prefix partial (read by the peers)
 
-    if (bid >= chan_blocks) {
-        // Tail part: per-rank expert offsets; warp 0 also the partition bases.
-        const int64_t gw = (bid - chan_blocks) * wpb + warp;
-        if (gw >= P) return;
-        const int epr = E / P;
-        const int64_t d = gw;
+    const int epr = a.epr;
+    const int G = (P + 3) >> 2;  // rank groups of 4
+    const int32_t gw = r * kNotifyWarps + warp;
+    const int32_t sb = gw * a.wq + min(gw, a.wr);
+    const int32_t se = sb + a.wq + (gw < a.wr ? 1 : 0);
+    const int32_t cq = a.cq, cr = a.cr;
+    const uint8_t* src_rows = itr + static_cast<int64_t>(s) * T * P;
+
+    // --- every load that does not wait on another, issued first -----------
+    // (a) rank-prefix partial: rows [pb, pe) of the source ranks before s,
+    //     4 ranks per thread (A4) and rpp rows per pass.
+    const int32_t sq = s >> a.lcs, sr = s & (cs - 1);
+    const int32_t pb = r * sq + min(r, sr);
+    const int32_t pe = pb + sq + (r < sr ? 1 : 0);
+    const int cols = A4 ? P >> 2 : P;
+    const int rpp = max(1, min(cols >= kNotifyThreads ? 1 : kNotifyThreads / cols, pe - pb));
+    int4 racc = make_int4(0, 0, 0, 0);
+    if (cols <= kNotifyThreads && tid < rpp * cols) {
+        const int cg = tid % cols;
+#pragma unroll 8
+        for (int32_t q = pb + tid / cols; q < pe; q += rpp) {
+            if (A4) {
+                const int4 v = __ldg(reinterpret_cast<const int4*>(ntpr + static_cast<int64_t>(q) * P) + cg);
+                racc.x += v.x;
+                racc.y += v.y;
+                racc.z += v.z;
+                racc.w += v.w;
+            } else {
+                racc.x += __ldg(ntpr + static_cast<int64_t>(q) * P + cg);
+            }
+        }
+    }
+    // (b) receive counts of rank s's experts: this CTA's share [lb, le) of
+    //     them, one warp per expert (the first 8 loaded here), lanes over the
+    //     source ranks.
+    const int32_t lb = r * a.eq + min(r, a.er);
+    const int32_t le = lb + a.eq + (r < a.er ? 1 : 0);
+    const int32_t* ecol = ntpe + static_cast<int64_t>(s) * epr;  // rank s's experts in row 0
+    int32_t esum = 0;
+    if (lb + warp < le)
+        for (int q = lane; q < P; q += 32) esum += __ldg(ecol + static_cast<int64_t>(q) * E + lb + warp);
+    // --- 1. count ---------------------------------------------------------
+    // With one block of rank groups and at most kNotifyCache steps per warp,
+    // a lane's flag words stay in registers for the second pass.
+    uint32_t fc[kNotifyCache];
+    bool cached = false;
+    for (int rb = 0; rb * 32 < G; ++rb) {
+        const int gn = min(32, G - rb * 32);
+        int L = 1;
+        while (L < gn) L <<= 1;
+        const int tpw = 32 / L;
+        const int g = lane & (L - 1), tk = lane / L;
+        const int d = 4 * (rb * 32 + g);
+        int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+        cached = G <= 32 && se - sb <= kNotifyCache * tpw;
+        if (cached) {
+#pragma unroll
+            for (int i = 0; i < kNotifyCache; ++i) {
+                const int32_t t = sb + tk + i * tpw;
+                fc[i] = (g < gn && t < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < kNotifyCache; ++i) {
+                c0 += byte_of(fc[i], 0);
+                c1 += byte_of(fc[i], 1);
+                c2 += byte_of(fc[i], 2);
+                c3 += byte_of(fc[i], 3);
+            }
+        } else if (g < gn) {
+#pragma unroll 4
+            for (int32_t t = sb + tk; t < se; t += tpw) {
+                const uint32_t f = load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P);
+                c0 += byte_of(f, 0);
+                c1 += byte_of(f, 1);
+                c2 += byte_of(f, 2);
+                c3 += byte_of(f, 3);
+            }
+        }
+        for (int o = L; o < 32; o <<= 1) {
+            c0 += __shfl_xor_sync(0xffffffffu, c0, o);
+            c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+            c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+            c3 += __shfl_xor_sync(0xffffffffu, c3, o);
+        }
+        if (tk == 0 && g < gn) {
+            int32_t* wc = wcnt + warp * P + d;
+            wc[0] = c0;
+            if (d + 1 < P) wc[1] = c1;
+            if (d + 2 < P) wc[2] = c2;
+            if (d + 3 < P) wc[3] = c3;
+        }
+    }
+    if (cols <= kNotifyThreads && tid < rpp * cols) tmp_r[tid] = racc;
+    MOE_STAMP(1);
+    __syncthreads();
+    MOE_STAMP(2);
+
+    // --- 2. block totals, exclusive warp offsets, partials -----------------
+    for (int d = tid; d < P; d += kNotifyThreads) {
+        int32_t run = 0;
+        for (int w = 0; w < kNotifyWarps; ++w) {
+            const int32_t v = wcnt[w * P + d];
+            wcnt[w * P + d] = run;
+            run += v;
+        }
+        ctot[d] = run;
+        int32_t rp = 0;
+        if (cols <= kNotifyThreads) {
+            const int cg = A4 ? d >> 2 : d, j = A4 ? d & 3 : 0;
+            for (int k = 0; k < rpp; ++k) {
+                const int4 v = tmp_r[k * cols + cg];
+                rp += j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+            }
+        } else {
+            for (int32_t q = pb; q < pe; ++q) rp += __ldg(ntpr + static_cast<int64_t>(q) * P + d);
+        }
+        rpart[d] = rp;
+    }
+    for (int32_t l = lb + warp; l < le; l += kNotifyWarps) {
+        int32_t sum = esum;
+        if (l != lb + warp) {
+            sum = 0;
+            for (int q = lane; q < P; q += 32) sum += __ldg(ecol + static_cast<int64_t>(q) * E + l);
+        }
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) ecnt[l] = (sum + A - 1) / A * A;  // fits int32 (shape limits)
+    }
+    MOE_STAMP(3);
+    cluster_sync_all();
+    MOE_STAMP(4);
+    // Every (rank, peer CTA) pair read by its own thread, then summed locally.
+    for (int i = tid; i < P * cs; i += kNotifyThreads) {
+        const int q = i / P, d = i - q * P;
+        if (q != r) {
+            xc[q * P + d] = ld_cluster_s32(cluster_map(xc + q * P + d, q));
+            xr[q * P + d] = ld_cluster_s32(cluster_map(xr + q * P + d, q));
+        }
+    }
+    if (r == 0 && warp == kNotifyWarps - 1) {
+        // Rank s's per-expert counts from the CTAs that summed them, scanned.
+        const int32_t eq = a.eq, er = a.er;
         int32_t carry = 0;
         for (int l0 = 0; l0 < epr; l0 += 32) {
             const int l = l0 + lane;
-            const int32_t v = l < epr ? __ldg(nrtpe + d * epr + l) : 0;
+            int32_t v = 0;
+            if (l < epr) {
+                const int owner = l < er * (eq + 1) ? l / (eq + 1) : er + (l - er * (eq + 1)) / eq;
+                v = owner == 0 ? ecnt[l] : ld_cluster_s32(cluster_map(ecnt + l, owner));
+            }
             const int32_t incl = warp_inclusive_scan(v, lane);
-            if (l < epr) reo[d * epr + l] = carry + incl - v;
+            if (l < epr) {
+                nrtpe[s * epr + l] = v;
+                reo[s * epr + l] = carry + incl - v;
+            }
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (gw == 0) {
-            int64_t run = 0;
-            for (int d0 = 0; d0 < P; d0 += 32) {
-                const int dd = d0 + lane;
-                const int64_t v = dd < P ? __ldg(nrt + dd) : 0;
-                const int64_t incl = warp_inclusive_scan(v, lane);
-                if (dd < P) part_row_base[dd] = run + incl - v;
-                run += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) part_row_base[P] = run;
-        }
-        return;
     }
-
-    if (rank_major) {
-        const int64_t ch = bid * wpb + warp;
-        if (ch >= static_cast<int64_t>(P) * C) return;
-        const int64_t s = ch / C, c = ch % C;
-        int64_t b, e;
-        split_range(T, C, c, &b, &e);
-        for (int d0 = 0; d0 < P; d0 += 128) {
-            const int d = d0 + 4 * lane;
-            if (d >= P) continue;
-            int4 pre = make_int4(0, 0, 0, 0);
+    cluster_arrive();  // done reading the peers; their shared memory may go at the final wait
+    __syncthreads();
+    for (int d = tid; d < P; d += kNotifyThreads) {
+        int32_t before = 0, all = 0, rp = 0;
 #pragma unroll 4
-            for (int64_t cc = 0; cc < c; ++cc) {
-                const int4 v = __ldg(reinterpret_cast<const int4*>(ccount + (s * C + cc) * P + d));
-                pre.x += v.x;
-                pre.y += v.y;
-                pre.z += v.z;
-                pre.w += v.w;
-            }
-            const int4 cnt = __ldg(reinterpret_cast<const int4*>(ccount + ch * P + d));
-            const int4 rb = s > 0 ? __ldg(reinterpret_cast<const int4*>(rpm + (s - 1) * P + d))
-                                  : make_int4(0, 0, 0, 0);
-            cpm[(s * P + d + 0) * C + c] = pre.x + cnt.x;
-            cpm[(s * P + d + 1) * C + c] = pre.y + cnt.y;
-            cpm[(s * P + d + 2) * C + c] = pre.z + cnt.z;
-            cpm[(s * P + d + 3) * C + c] = pre.w + cnt.w;
-            int32_t b0 = rb.x + pre.x, b1 = rb.y + pre.y, b2 = rb.z + pre.z, b3 = rb.w + pre.w;
-            rcpm[(static_cast<int64_t>(d + 0) * P + s) * C + c] = b0;
-            rcpm[(static_cast<int64_t>(d + 1) * P + s) * C + c] = b1;
-            rcpm[(static_cast<int64_t>(d + 2) * P + s) * C + c] = b2;
-            rcpm[(static_cast<int64_t>(d + 3) * P + s) * C + c] = b3;
-#pragma unroll 8
-            for (int64_t t = b; t < e; ++t) {
-                const int64_t g = s * T + t;
-                const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(itr + g * P + d));
-                int4 v;
-                v.x = flag(w, 0) ? b0++ : -1;
-                v.y = flag(w, 1) ? b1++ : -1;
-                v.z = flag(w, 2) ? b2++ : -1;
-                v.w = flag(w, 3) ? b3++ : -1;
-                *reinterpret_cast<int4*>(send_head + g * P + d) = v;
-            }
+        for (int q = 0; q < cs; ++q) {
+            const int32_t v = xc[q * P + d];
+            before += q < r ? v : 0;
+            all += v;
+            rp += xr[q * P + d];
         }
-        return;
-    }
-
-    // Token-major channel heads.
-    int32_t* base = sm;      // [P]   next free row of d for this channel
-    int32_t* woff = sm + P;  // [warps][P]
-    const int64_t s = bid / C, c = bid % C;
-    int64_t b, e;
-    split_range(T, C, c, &b, &e);
-    for (int d = tid; d < P; d += nthreads) {
-        int32_t pre = 0;
-#pragma unroll 8
-        for (int64_t cc = 0; cc < c; ++cc) pre += ccount[(s * C + cc) * P + d];
-        const int32_t cnt = ccount[(s * C + c) * P + d];
-        cpm[(s * P + d) * C + c] = pre + cnt;
-        const int32_t rank_base = s > 0 ? rpm[(s - 1) * P + d] : 0;
-        rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rank_base + pre;
-        base[d] = rank_base + pre;
+        base[d] = before;
+        total[d] = all;
+        rprev[d] = rp;
     }
     __syncthreads();
-    int32_t* mine = woff + warp * P;
-    for (int64_t t0 = b; t0 < e; t0 += nthreads) {
-        const int64_t t = t0 + tid;
-        const bool active = t < e;
-        const int64_t g = s * T + (active ? t : b);
-        const uint8_t* row = itr + g * P;
-        for_each_rank_ballot(row, active, P, [&](int d, uint32_t bal) {
-            if (lane == (d & 31)) mine[d] = __popc(bal);
-        });
-        __syncthreads();
-        for (int d = tid; d < P; d += nthreads) {
-            int32_t run = base[d];
-            for (int w = 0; w < wpb; ++w) {
-                const int32_t cnt = woff[w * P + d];
-                woff[w * P + d] = run;
-                run += cnt;
+    MOE_STAMP(5);
+
+    // --- 3. heads ------------------------------------------------------------
+    // Channels that start inside this CTA's tokens [cta_b, cta_e): their
+    // counts go to chv (written out coalesced below) when they fit.
+    const int32_t cta_b = r * kNotifyWarps * a.wq + min(r * kNotifyWarps, a.wr);
+    const int32_t cta_e = min(T, cta_b + kNotifyWarps * a.wq + max(0, min(kNotifyWarps, a.wr - r * kNotifyWarps)));
+    const int32_t nonempty = min(T, C);  // channels that start before T
+    const int32_t c_lo = cta_b < T ? next_channel(cta_b, cq, cr) : nonempty;
+    const int32_t c_hi = cta_e < T ? next_channel(cta_e, cq, cr) : nonempty;
+    const bool buffered = static_cast<int64_t>(c_hi - c_lo) * P <= kNotifyChanBuf;
+    for (int rb = 0; rb * 32 < G; ++rb) {
+        const int gn = min(32, G - rb * 32);
+        int L = 1;
+        while (L < gn) L <<= 1;
+        const int tpw = 32 / L;
+        const int g = lane & (L - 1), tk = lane / L;
+        const int d = 4 * (rb * 32 + g);
+        const bool gvalid = g < gn;
+        const int last = (tpw - 1) * L + g;  // lane of this group's last token in a step
+        int run[4], rp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool ok = gvalid && d + j < P;
+            run[j] = ok ? base[d + j] + wcnt[warp * P + d + j] : 0;
+            rp[j] = ok ? rprev[d + j] : 0;
+        }
+        // Next channel start at or after this lane's token (nb = T: none).
+        int32_t nc = sb + tk < se ? next_channel(sb + tk, cq, cr) : C;
+        int32_t nb = channel_begin(nc, cq, cr);
+        // One step: tpw tokens, this lane's token t and flags f.
+        auto step = [&](int32_t t, uint32_t f) {
+            const bool tv = gvalid && t < se;
+            // Inclusive counts over this step's tokens, 4 ranks per word.
+            uint32_t incl = f;
+            for (int o = L; o < 32; o <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
             }
-            base[d] = run;
-        }
-        __syncthreads();
-        const uint32_t below = lanemask_lt();
-        int32_t* out = send_head + g * P;
-        if ((P & 3) == 0) {
-            int4 pack;
-            for_each_rank_ballot(row, active, P, [&](int d, uint32_t bal) {
-                const bool has = (bal >> lane) & 1u;
-                const int32_t v = has ? mine[d] + __popc(bal & below) : -1;
-                switch (d & 3) {
-                    case 0: pack.x = v; break;
-                    case 1: pack.y = v; break;
-                    case 2: pack.z = v; break;
-                    default:
-                        pack.w = v;
-                        if (active) *reinterpret_cast<int4*>(out + (d - 3)) = pack;
+            const uint32_t excl = incl - f;
+            const uint32_t step_total = L == 32 ? f : __shfl_sync(0xffffffffu, incl, last);
+            if (tv) {
+                int loc[4], v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    loc[j] = run[j] + byte_of(excl, j);
+                    v[j] = byte_of(f, j) ? rp[j] + loc[j] : -1;
                 }
-            });
-        } else {
-            for_each_rank_ballot(row, active, P, [&](int d, uint32_t bal) {
-                const bool has = (bal >> lane) & 1u;
-                if (active) out[d] = has ? mine[d] + __popc(bal & below) : -1;
-            });
+                int32_t* out = send_head + (static_cast<int64_t>(s) * T + t) * P + d;
+                if (A4) {
+                    *reinterpret_cast<int4*>(out) = make_int4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (d + j < P) out[j] = v[j];
+                }
+                while (nb < t) nb = channel_begin(++nc, cq, cr);
+                if (nb == t) {  // t starts channel nc
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (d + j < P) {
+                            if (buffered) {
+                                chv[(nc - c_lo) * P + d + j] = loc[j];
+                            } else {
+                                rcpm[(static_cast<int64_t>(d + j) * P + s) * C + nc] = rp[j] + loc[j];
+                                if (nc > 0) cpm[(static_cast<int64_t>(s) * P + d + j) * C + nc - 1] = loc[j];
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) run[j] += byte_of(step_total, j);
+        };
+        // One copy of the step code: flags from the registers of the count
+        // pass (selected without indexing) or read again.
+#pragma unroll 1
+        for (int32_t i = 0, t0 = sb; t0 < se; ++i, t0 += tpw) {
+            const int32_t t = t0 + tk;
+            uint32_t f;
+            if (cached) {
+                f = i == 0 ? fc[0] : (i == 1 ? fc[1] : (i == 2 ? fc[2] : fc[3]));
+            } else {
+                f = (gvalid && t < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P) : 0u;
+            }
+            step(t, f);
         }
-        __syncthreads();
     }
+    if (buffered) {
+        __syncthreads();
+        // recv_channel_prefix_matrix[d][s][c] and channel_prefix_matrix[s][d][c-1]
+        // for the channels starting here: c runs fastest, so consecutive
+        // threads write consecutive entries of a row.
+        const int nch = c_hi - c_lo;
+        for (int i = tid; i < nch * P; i += kNotifyThreads) {
+            const int d = i / nch, k = i - d * nch;
+            const int32_t c = c_lo + k;
+            const int32_t v = chv[k * P + d];
+            rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rprev[d] + v;
+            if (c > 0) cpm[(static_cast<int64_t>(s) * P + d) * C + c - 1] = v;
+        }
+    }
+
+    MOE_STAMP(6);
+    // --- 4. per-rank outputs ------------------------------------------------
+    if (r == cs - 1) {
+        // Channels that end at T (the last, and empty trailing ones when T < C)
+        // and channels that start at T (empty ones).
+        const int32_t cl = T < C ? (T > 0 ? T - 1 : 0) : C - 1;
+        const int32_t cb = T < C ? T : C;
+        for (int d = tid; d < P; d += kNotifyThreads) {
+            const int32_t tot = total[d], rp = rprev[d];
+            rpm[s * P + d] = rp + tot;
+            for (int32_t c = cl; c < C; ++c) cpm[(static_cast<int64_t>(s) * P + d) * C + c] = tot;
+            for (int32_t c = cb; c < C; ++c) rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rp + tot;
+            if (s == P - 1) {
+                nrt[d] = rp + tot;
+                nrt64[d] = rp + tot;
+            }
+        }
+        if (s == P - 1) {
+            __syncthreads();
+            if (warp == 0) {
+                int64_t run = 0;
+                for (int d0 = 0; d0 < P; d0 += 32) {
+                    const int dd = d0 + lane;
+                    const int64_t v = dd < P ? nrt64[dd] : 0;
+                    const int64_t incl = warp_inclusive_scan(v, lane);
+                    if (dd < P) part_row_base[dd] = run + incl - v;
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
+                if (lane == 0) part_row_base[P] = run;
+            }
+        }
+    }
+    cluster_wait();
+    MOE_STAMP(7);
+    MOE_PROF_END();
+}
+
+struct NotifyPlan {
+    int cluster;
+    size_t smem;
+};
+
+NotifyPlan notify_plan(const moe_shape& s) {
+    const int64_t T = s.S / s.P;
+    // Tokens a warp covers per step in the first block of rank groups.
+    const int G = (s.P + 3) / 4;
+    int L = 1;
+    while (L < (G < 32 ? G : 32)) L <<= 1;
+    const int64_t tpw = 32 / L;
+    // Fewest steps per warp (one if possible), with the grid within about
+    // one wave of 4 CTAs per SM; a power of two.
+    int c = 1;
+    while (c < kNotifyMaxCluster && static_cast<int64_t>(c) * kNotifyWarps * tpw < T) c <<= 1;
+    const int64_t wave = 4 * static_cast<int64_t>(device_sm_count());
+    while (c > 1 && static_cast<int64_t>(c) * s.P > wave) c >>= 1;
+    // the peers' totals and partials (2 x cs x P int32) stay within 64 KB
+    while (c > 1 && static_cast<int64_t>(c) * s.P * 8 > 64 * 1024) c >>= 1;
+    NotifyPlan p;
+    p.cluster = c;
+    p.smem = notify_smem(s.P, s.E, c).bytes;
+    return p;
 }
 
 }  // namespace
 
+MOE_PROFILE_UNIT(notify)
+
 int64_t notify_scratch_bytes(const moe_shape& s) {
-    return round_up(static_cast<int64_t>(s.P) * s.num_channels * s.P * 4, 256);
+    (void)s;
+    return 0;
 }
 
 cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t* ntpe,
                           const uint8_t* itr, int32_t* rpm, int32_t* cpm, int32_t* rcpm,
                           int32_t* nrt, int32_t* nrtpe, int32_t* reo, int32_t* send_head,
                           int64_t* part_row_base, void* scratch, cudaStream_t stream) {
+    (void)scratch;
     const int64_t T = s.S / s.P;
     const NotifyPlan p = notify_plan(s);
-    int32_t* ccount = static_cast<int32_t*>(scratch);
-    const size_t smem_count = p.rank_major ? 0 : static_cast<size_t>(p.wpb) * s.P * 4;
-    const size_t smem_head = p.rank_major ? 0 : static_cast<size_t>(p.wpb + 1) * s.P * 4;
-    cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(notify_count_kernel), smem_count, p.threads,
-                                   nullptr);
+    const bool a4 = (s.P & 3) == 0;
+    const void* fn = a4 ? reinterpret_cast<const void*>(notify_kernel<true>)
+                        : reinterpret_cast<const void*>(notify_kernel<false>);
+    cudaError_t e = prepare_kernel(fn, p.smem, kNotifyThreads, nullptr);
     if (e != cudaSuccess) return e;
-    e = prepare_kernel(reinterpret_cast<const void*>(notify_head_kernel), smem_head, p.threads, nullptr);
-    if (e != cudaSuccess) return e;
-    const int64_t grid1 = p.chan_blocks + p.rank_blocks + p.expert_blocks;
-    e = launch_pdl(notify_count_kernel, static_cast<unsigned>(grid1), p.threads, smem_count, stream, s.P,
-                   s.E, s.num_channels, s.expert_alignment, T, p.rank_major, p.chan_blocks, p.rank_blocks,
-                   ntpr, ntpe, itr, rpm, nrt, nrtpe, ccount);
-    if (e != cudaSuccess) return e;
-    const int64_t grid2 = p.chan_blocks + p.tail_blocks;
-    return launch_pdl(notify_head_kernel, static_cast<unsigned>(grid2), p.threads, smem_head, stream, s.P, s.E,
-                      s.num_channels, T, p.rank_major, p.chan_blocks, itr, static_cast<const int32_t*>(rpm),
-                      static_cast<const int32_t*>(nrt), static_cast<const int32_t*>(nrtpe),
-                      static_cast<const int32_t*>(ccount), cpm, rcpm, send_head, reo, part_row_base);
+    const int cs = cluster_size_for(fn, p.cluster, kNotifyThreads, p.smem);
+    if (cs < 1) return cudaErrorInvalidConfiguration;
+    auto kern = a4 ? notify_kernel<true> : notify_kernel<false>;
+    const size_t smem = notify_smem(s.P, s.E, cs).bytes;  // for the cluster size granted
+    NotifyParams a{};
+    a.P = s.P;
+    a.E = s.E;
+    a.C = s.num_channels;
+    a.A = s.expert_alignment;
+    a.epr = s.E / s.P;
+    a.T = static_cast<int32_t>(T);
+    a.cs = cs;
+    a.lcs = 0;
+    while ((1 << a.lcs) < cs) ++a.lcs;
+    a.wq = static_cast<int32_t>(T / (cs * kNotifyWarps));
+    a.wr = static_cast<int32_t>(T % (cs * kNotifyWarps));
+    a.cq = static_cast<int32_t>(T / s.num_channels);
+    a.cr = static_cast<int32_t>(T % s.num_channels);
+    a.eq = a.epr / cs;
+    a.er = a.epr % cs;
+    a.ntpr = ntpr;
+    a.ntpe = ntpe;
+    a.itr = itr;
+    a.rpm = rpm;
+    a.cpm = cpm;
+    a.rcpm = rcpm;
+    a.nrt = nrt;
+    a.nrtpe = nrtpe;
+    a.reo = reo;
+    a.send_head = send_head;
+    a.part_row_base = part_row_base;
+    return launch_pdl_cluster(kern, static_cast<unsigned>(s.P) * cs, kNotifyThreads, smem, cs, stream, a);
 }
 
 }  // namespace moe

@@ -13,7 +13,9 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe.so")
+# MOE_LIBRARY=NAME loads the build variant libmoe_NAME.so (build.py) instead.
+LIB_PATH = os.path.join(_HERE, f"libmoe_{os.environ['MOE_LIBRARY']}.so" if os.environ.get("MOE_LIBRARY")
+                        else "libmoe.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -35,7 +37,7 @@ MOE_RUN_FUSED = 1
 MOE_RUN_EXPERT = 2
 
 # Bytes of the scratch buffer built into the library (include/moe.h).
-MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
+MOE_LAYOUT_STATIC_SCRATCH_BYTES = 1024 * 4
 
 
 class MoeError(RuntimeError):

@@ -337,21 +337,28 @@ moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_to
  * that cannot allocate device memory, such as code hosted by an engine that
  * owns all device memory and forbids allocation after start-up, or serving
  * loops where cudaMalloc would stall the device. Inputs, outputs and results
- * are those of moe_layout; the per-block partial counts go to a buffer of
+ * are those of moe_layout; the one scratch array moe_layout needs (an
+ * out-of-range flag per source rank, folded into err) is a buffer of
  * MOE_LAYOUT_STATIC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits.
- *   - Shapes whose partials need more than MOE_LAYOUT_STATIC_SCRATCH_BYTES
- *     (moe_scratch_bytes is an upper bound) return MOE_ERR_UNSUPPORTED and
- *     enqueue nothing.
+ *   - The buffer holds the flags of the largest shape moe_check_shape
+ *     accepts (MOE_MAX_RANKS source ranks). A shape needing more is refused
+ *     with MOE_ERR_UNSUPPORTED before anything is enqueued (moe_check_shape
+ *     already refuses every such shape the same way).
  *   - The first call on each device looks up the buffer's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *     (with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture. The kept address
+ *     assumes the device's primary context is never reset or destroyed
+ *     (cudaDeviceReset): after a reset, do not call this entry point again
+ *     in the same process.
  *   - All calls share the buffer, which keeps the last call's contents;
- *     nothing in it needs to start at zero. Calls that overlap on the GPU
- *     (different streams or threads) race on it: serialise them.
+ *     every flag is written before it is read, so nothing needs to start at
+ *     zero. Calls that overlap on the GPU (different streams or threads)
+ *     race on it: serialise them. Calls enqueued one after another on one
+ *     stream are serialised by the stream.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
-#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (1u << 20)
+#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (MOE_MAX_RANKS * 4u)
 moe_status moe_layout_static_scratch(const moe_shape* shape, const int32_t* topk_idx,
                                      int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
                                      uint8_t* is_token_in_rank, uint32_t* is_token_in_rank_bits,
@@ -405,6 +412,35 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
                         const int32_t* const* topk_idx_host, const float* const* topk_weights_host,
                         uint16_t* const* out_host, const void* y, int64_t y_row_stride, int32_t flags,
                         void* workspace, int64_t workspace_bytes, int32_t* err_host);
+
+/*
+ * moe_profile_attach -- profile builds only (compiled with -DMOE_PROFILE into
+ * libmoe_profile.so; the default libmoe.so has no such symbol and its kernels
+ * record nothing). The pages' "Ascend DeepEP MoE Dispatch Optimization",
+ * section "Device 侧计时": per-core phase times written to exclusive slots
+ * behind a compile-time switch that costs nothing when off.
+ *
+ * Points every instrumented kernel at `slots`, a device array of
+ * MOE_PROF_KERNELS * MOE_PROF_CTAS * MOE_PROF_PHASES uint64 (bytes >= that
+ * times 8, 16-byte aligned), or detaches them (slots = NULL). Thereafter CTA b
+ * of kernel k writes row (k * MOE_PROF_CTAS + b) * MOE_PROF_PHASES:
+ *   slot 0: %globaltimer (ns) when the CTA starts its work (after waiting for
+ *           the previous kernel on the stream);
+ *   slot p >= 1: the CTA's clock64 cycles from then to the end of phase p,
+ *           or, for the int8 consumer's per-token steps, that step's cycles
+ *           summed over the CTA's first consumer warp's tokens (added to:
+ *           clear the array before a run).
+ * Kernel ids: 0 layout, 1 notify, 2 dispatch bf16, 3 dispatch int8,
+ * 4 combine, 5 fused, 6 notify_expert. CTAs at or beyond MOE_PROF_CTAS record
+ * nothing. Synchronous (a copy to each kernel unit's device pointer); call it
+ * with no work of this library in flight. Outputs are unchanged.
+ */
+#define MOE_PROF_KERNELS 8
+#define MOE_PROF_CTAS 4096
+#define MOE_PROF_PHASES 16
+#ifdef MOE_PROFILE
+moe_status moe_profile_attach(void* slots, int64_t bytes);
+#endif
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -18,12 +18,16 @@ def lib():
     return moe.lib()
 
 
-def _declared():
+def _declared(profile=False):
+    """Entry points declared in include/*.h; those under #ifdef MOE_PROFILE
+    only when profile is set."""
     names = set()
     for fn in os.listdir(os.path.join(ROOT, "include")):
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            if not profile:
+                text = re.sub(r"#ifdef MOE_PROFILE.*?#endif", "", text, flags=re.S)
             names |= set(re.findall(r"\b(moe_\w+)\s*\(", text))
     return names
 
@@ -34,6 +38,18 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(moe.EXPORTS) >= names
+
+
+def test_profile_entry_point_only_in_the_profile_build(lib):
+    """The default library carries no profile symbol; the -DMOE_PROFILE build
+    exports moe_profile_attach next to every other entry point."""
+    import ctypes
+
+    assert not hasattr(lib, "moe_profile_attach")
+    assert "moe_profile_attach" in _declared(profile=True) - _declared()
+    prof = ctypes.CDLL(moe_build.build(variant="profile"))
+    for n in _declared(profile=True):
+        assert hasattr(prof, n), n
 
 
 def test_slot_stride_and_limits(lib):
@@ -72,14 +88,16 @@ def test_null_pointers_rejected_before_any_launch(lib):
 
 
 def test_static_scratch_size_guard_runs_on_the_host(lib):
-    """moe_layout_static_scratch refuses shapes beyond its built-in buffer before
-    touching any device (the fake pointers below are never dereferenced)."""
-    big = moe.make_shape(1024, 4096, 1024 * 64, 8, 64)
-    assert moe.moe_scratch_bytes(big) > moe.MOE_LAYOUT_STATIC_SCRATCH_BYTES
+    """moe_layout_static_scratch's built-in buffer holds one flag per source rank
+    of the largest accepted shape; larger shapes are refused before any device
+    is touched (the fake pointers below are never dereferenced)."""
+    assert moe.MOE_LAYOUT_STATIC_SCRATCH_BYTES == 4 * 1024  # MOE_MAX_RANKS int32 flags
+    too_big = moe.make_shape(2048, 4096, 2048 * 64, 8, 64)
     fake = 1 << 20
-    assert lib.moe_layout_static_scratch(big, fake, fake, fake, fake, fake, fake,
+    assert lib.moe_layout_static_scratch(too_big, fake, fake, fake, fake, fake, fake,
                                          None) == moe.MOE_ERR_UNSUPPORTED
-    assert lib.moe_layout_static_scratch(big, None, fake, fake, fake, None, None,
+    ok = moe.make_shape(1024, 4096, 1024 * 64, 8, 64)
+    assert lib.moe_layout_static_scratch(ok, None, fake, fake, fake, None, None,
                                          None) == moe.MOE_ERR_INVALID_ARG
 
 

@@ -43,6 +43,17 @@ def test_reference_arm_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the config is what was timed: here the whole tiny workload fits the budget
+    assert d["config"]["sample"] == "full workload" and d["config"]["S"] == 256
+    assert "T=64 tokens per rank (S=256" in cb["sample"]
+
+
+def test_reference_arm_states_a_reduced_sample():
+    """With --ref-tokens below the workload's own T, the config names the
+    tokens per rank that were timed."""
+    d = _bench("--impl", "reference", "--workload", "tiny_p4_e16_h256", "--steps", "2", "--warmup", "3",
+               "--ref-tokens", "16")
+    assert d["config"]["S"] == 4 * 16 and d["config"]["sample"].startswith("T=16 of the workload's 64")
 
 
 @pytest.mark.gpu
@@ -61,5 +72,7 @@ def test_gpu_arm_line():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert e2e["value"] != d["value"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
-    assert d["gpu_launches"] == 6 * 20
+    assert d["gpu_launches"] == 5 * 20
+    st = d["stages"]
+    assert st["layout_notify_us"] >= 0 and st["layout_notify_event_us"] > 0 and st["layout_notify_method"]
     assert "l2" in d["config"]

@@ -3,11 +3,12 @@
 Some callers of the library cannot allocate device memory -- code hosted by an
 engine that owns all device memory and forbids allocation after start-up, or
 serving loops where cudaMalloc would stall the device. For them the library
-keeps the layout's scratch in a buffer compiled into it. These checks call that
-entry point through the C ABI and compare it with moe_layout (which takes a
-caller-allocated scratch buffer) on two calls in a row with different
-routings, so the second call cannot pass on what the first one left behind.
-Layout outputs are integers: the comparison is bit-exact.
+keeps the layout's scratch (one out-of-range flag per source rank) in a buffer
+compiled into it. These checks call that entry point through the C ABI and
+compare it with moe_layout (which takes a caller-allocated scratch buffer) and
+with the oracle, on calls in a row with different routings, so no call can
+pass on what an earlier one left behind in the shared buffer. Layout outputs
+are integers: the comparison is bit-exact.
 """
 
 import ctypes
@@ -15,6 +16,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from combine_moe_layout_02_gb300 import inputs, moe
 
 pytestmark = pytest.mark.gpu
@@ -44,39 +46,78 @@ def _call_static(shape, idx, o, stream):
         ctypes.c_void_p(o["err"].data_ptr()), ctypes.c_void_p(stream))
 
 
-def test_static_scratch_layout_matches_moe_layout_twice():
+def _check_against_oracle(w, got):
+    lay = oracle.layout(w.P, w.E, w.topk_idx)
+    for k in ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank"):
+        np.testing.assert_array_equal(got[k].cpu().numpy(), lay[k], err_msg=k)
+    bits = np.zeros((w.S, (w.P + 31) // 32), dtype=np.uint32)
+    for d in range(w.P):
+        bits[:, d // 32] |= lay["is_token_in_rank"][:, d].astype(np.uint32) << np.uint32(d % 32)
+    np.testing.assert_array_equal(got["is_token_in_rank_bits"].cpu().numpy().view(np.uint32), bits)
+
+
+def test_static_scratch_layout_matches_moe_layout_and_oracle():
     import torch
 
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev).cuda_stream
-    cases = [inputs.workload("p128_e256_t512_h7168_zipf", with_x=False, seed=0),
-             inputs.workload("p8_e256_t4096_h7168", with_x=False, seed=1)]
-    for w in cases:
-        shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0)
-        # Both shapes' layout partials fit the built-in buffer (the static call
-        # below would otherwise return MOE_ERR_UNSUPPORTED); moe_scratch_bytes is
-        # larger, as it also covers the other entry points' scratch.
-        idx = torch.from_numpy(w.topk_idx).to(dev)
+    # Three static calls in a row on one stream. The second has another shape;
+    # the third repeats the first shape with another routing and is enqueued
+    # directly behind the second, with no synchronisation in between.
+    ws = [inputs.workload("p128_e256_t512_h7168_zipf", with_x=False, seed=0),
+          inputs.workload("p8_e256_t4096_h7168", with_x=False, seed=1),
+          inputs.workload("p128_e256_t512_h7168_zipf", with_x=False, seed=5)]
+    shapes = [moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0) for w in ws]
+    idxs = [torch.from_numpy(w.topk_idx).to(dev) for w in ws]
+    refs = []
+    for w, shape, idx in zip(ws, shapes, idxs):
         ref = _outputs(shape, dev)
         scratch = torch.empty(moe.moe_scratch_bytes(shape), dtype=torch.uint8, device=dev)
         moe.moe_layout(shape, idx, ref["num_tokens_per_rank"], ref["num_tokens_per_expert"],
                        ref["is_token_in_rank"], ref["is_token_in_rank_bits"], ref["err"], scratch)
-        got = _outputs(shape, dev)
-        assert _call_static(shape, idx, got, stream) == moe.MOE_OK
-        torch.cuda.synchronize(dev)
+        refs.append(ref)
+    torch.cuda.synchronize(dev)
+    gots = [_outputs(shape, dev) for shape in shapes]
+    assert _call_static(shapes[0], idxs[0], gots[0], stream) == moe.MOE_OK
+    torch.cuda.synchronize(dev)
+    assert _call_static(shapes[1], idxs[1], gots[1], stream) == moe.MOE_OK
+    assert _call_static(shapes[2], idxs[2], gots[2], stream) == moe.MOE_OK
+    torch.cuda.synchronize(dev)
+    for w, ref, got in zip(ws, refs, gots):
         for k in ref:
             np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(), err_msg=k)
         assert int(got["err"][0].item()) == moe.MOE_OK
+        _check_against_oracle(w, got)
+
+
+def test_static_scratch_reports_out_of_range_ids():
+    """The flags in the shared buffer carry an out-of-range id into err, and the
+    next clean call on the same stream clears it again."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    w = inputs.workload("p32_e256_t128_h1024", with_x=False, seed=2)
+    shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0)
+    bad = w.topk_idx.copy()
+    bad[17, 3] = w.E  # one id past the last expert, on source rank 0
+    o_bad, o_ok = _outputs(shape, dev), _outputs(shape, dev)
+    assert _call_static(shape, torch.from_numpy(bad).to(dev), o_bad, stream) == moe.MOE_OK
+    assert _call_static(shape, torch.from_numpy(w.topk_idx).to(dev), o_ok, stream) == moe.MOE_OK
+    torch.cuda.synchronize(dev)
+    assert int(o_bad["err"][0].item()) == moe.MOE_ERR_TOPK_OUT_OF_RANGE
+    assert int(o_ok["err"][0].item()) == moe.MOE_OK
+    _check_against_oracle(w, o_ok)
 
 
 def test_static_scratch_rejects_shapes_beyond_its_buffer():
     import torch
 
     dev = torch.device("cuda", 0)
-    # P = 1024 ranks and E = 4096 experts with 64 tokens per rank need ~42 MB of partials.
-    shape = moe.make_shape(1024, 4096, 1024 * 64, 8, 64)
-    assert moe.moe_scratch_bytes(shape) > moe.MOE_LAYOUT_STATIC_SCRATCH_BYTES
-    o = _outputs(shape, dev)   # full-size outputs; the call must leave them untouched
+    # P = 2048 source ranks would need 8 KB of flags, past the 4 KB buffer
+    # (and past MOE_MAX_RANKS): refused before anything is enqueued.
+    shape = moe.make_shape(2048, 4096, 2048 * 4, 8, 64)
+    o = _outputs(moe.make_shape(4, 16, 64, 8, 64), dev)  # never written
     idx = torch.zeros((shape.S, shape.K), dtype=torch.int32, device=dev)
     st = _call_static(shape, idx, o, torch.cuda.current_stream(dev).cuda_stream)
     assert st == moe.MOE_ERR_UNSUPPORTED
