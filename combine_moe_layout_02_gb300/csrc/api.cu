@@ -527,6 +527,12 @@ moe_status moe_profile_attach(void* slots, int64_t bytes) {
 }
 #endif
 
+moe_status moe_test_fused_barrier(uint32_t spin_limit, int32_t skip_cta) {
+    if (spin_limit == 0) return MOE_ERR_INVALID_ARG;
+    arm_fused_barrier_test(spin_limit, skip_cta);
+    return MOE_OK;
+}
+
 moe_status moe_pad_partitions(const moe_shape* shape, const int32_t* num_recv_tokens,
                               const int64_t* part_row_base, void* recv_arena, int64_t arena_rows,
                               int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,

@@ -202,12 +202,14 @@ __device__ void drain_loads(uint64_t* bars, int stages, int64_t first, int64_t l
 template <bool EXPERT>
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchArgs a) {
     pdl_wait_then_release();
+    MOE_PROF_BEGIN(kProfDispatch);
     extern __shared__ __align__(128) unsigned char smem[];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     unsigned char* ring = smem + L.ring;
     load_prb_and_init(a, prb, bars);
+    MOE_STAMP(1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
@@ -286,11 +288,14 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
         }
         __syncwarp();
     }
+    MOE_STAMP(2);
     bulk_wait<0>();
+    MOE_STAMP(3);
     if (failed && lane == 0) {
         raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
         drain_loads(bars, NS, i, last_issued);
     }
+    MOE_PROF_END_N(4);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -414,6 +419,7 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
     // beside these slowed the pair down (measured: dispatch + combine 835 vs
     // 761 us at P=8, H=7168). The next kernel launches as these CTAs exit.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    MOE_PROF_BEGIN(kProfDispatchInt8);
     extern __shared__ __align__(128) unsigned char smem[];
     const DispatchSmem L = dispatch_smem(a.P, a.stages, a.row_bytes, true);
     int64_t* prb = reinterpret_cast<int64_t*>(smem + L.prb);
@@ -454,19 +460,29 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         // Loads still in flight land before the CTA may exit.
         const int64_t first = issued > NS ? issued - NS : 0;
         drain_loads(full, NS, first, issued - 1);
+        MOE_PROF_END_N(1);
         return;
     }
 
     const int cw = warp - 1;
     const int nchunks = a.H / 8;
     unsigned char* q = smem + L.qbuf + static_cast<size_t>(cw) * L.qstride;  // this warp's int8 row
+    // Profile build: consumer 0's cycles per step, summed over its tokens.
+    long long pw = 0, pa = 0, pq = 0, ps = 0, pn = 0;
+    (void)pw, (void)pa, (void)pq, (void)ps, (void)pn;
     for (int64_t i = cw; i < n_local; i += kInt8Consumers) {
         const int slot = static_cast<int>(i % NS);
         const int64_t g = blockIdx.x + i * G;
+        long long c_ = MOE_PROF_CLOCK();
         const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>((i / NS) & 1));
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
             break;
+        }
+        {
+            const long long c1 = MOE_PROF_CLOCK();
+            pw += c1 - c_;
+            c_ = c1;
         }
         const uint4* row = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * RB);
         __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
@@ -476,6 +492,11 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         const float scale = scale_of_amax(m);
         const bool zero = m == 0.f;
+        {
+            const long long c1 = MOE_PROF_CLOCK();
+            pa += c1 - c_;
+            c_ = c1;
+        }
         const float r = zero ? 0.f : __frcp_rn(scale);
         const bool fast = !zero && isfinite(r);
         // The previous token's stores have read the row buffer.
@@ -500,6 +521,11 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
         // Every lane has read the bf16 row: the slot goes back to the producer
         // now, so the next load overlaps this token's stores.
         __syncwarp();
+        {
+            const long long c1 = MOE_PROF_CLOCK();
+            pq += c1 - c_;
+            c_ = c1;
+        }
         if (lane == 0) mbar_arrive(&empty[slot]);
         fence_proxy_async_smem();
         __syncwarp();
@@ -526,8 +552,19 @@ __global__ void __launch_bounds__(kInt8Threads) dispatch_int8_kernel(const Dispa
             write_slot_meta(a, prb, g, lane);
         else
             write_token_meta(a, prb, g, lane, load_token_route(a, g, lane));
+        ps += MOE_PROF_CLOCK() - c_;
+        ++pn;
     }
     bulk_wait<0>();
+    if (cw == 0 && lane == 0) {
+        // slots: 1 wait for the row, 2 amax, 3 quantisation, 4 stores and
+        // metadata (cycles summed over the tokens), 5 tokens
+        MOE_PROF_PUT(1, pw);
+        MOE_PROF_PUT(2, pa);
+        MOE_PROF_PUT(3, pq);
+        MOE_PROF_PUT(4, ps);
+        MOE_PROF_PUT(5, pn);
+    }
 }
 
 }  // namespace

@@ -100,18 +100,24 @@ struct FusedArgs {
     int32_t* ecount;        // scratch [P*C][E]: slots of channel ch on expert e
     unsigned int* barrier;  // scratch, zeroed before launch
     int32_t* err;
+    uint32_t spin_limit;    // polls of a grid barrier before it gives up (kSpinLimit)
+    int64_t skip_arrival;   // CTA that leaves out its first arrival (test hook), else -1
 };
 
-// Bounded grid barrier over all CTAs of a cooperative launch. Returns false
-// (and records MOE_ERR_DEVICE_TIMEOUT) if the other CTAs did not arrive in time.
-__device__ bool grid_barrier(unsigned int* counter, unsigned int target, int32_t* err) {
+// Bounded grid barrier over all CTAs of a cooperative launch: at most
+// spin_limit polls. Returns false (and records MOE_ERR_DEVICE_TIMEOUT) if the
+// other CTAs did not arrive in time. skip_arrival (set only by the test hook
+// moe_test_fused_barrier) leaves this CTA's arrival out, so that every CTA's
+// wait runs out.
+__device__ bool grid_barrier(unsigned int* counter, unsigned int target, int32_t* err, uint32_t spin_limit,
+                             bool skip_arrival) {
     __shared__ int ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        atomicAdd(counter, 1u);
+        if (!skip_arrival) atomicAdd(counter, 1u);
         int done = 0;
-        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        for (uint32_t i = 0; i < spin_limit; ++i) {
             unsigned int v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
             if (v >= target) {
@@ -517,6 +523,7 @@ __global__ void fused_prep_kernel(unsigned int* counter) {
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_kernel(const FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait_then_release();
+    MOE_PROF_BEGIN(kProfFused);
     __shared__ int64_t prb[kMaxP + 1];
     const unsigned int n = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -545,18 +552,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_kernel(const Fused
     // status is raised after that barrier.
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.err) *a.err = 0;
     const bool bad = __syncthreads_or(phase_counts(a, region));
-    bool ok = grid_barrier(a.barrier, n, a.err);
+    MOE_STAMP(1);
+    bool ok = grid_barrier(a.barrier, n, a.err, a.spin_limit, blockIdx.x == a.skip_arrival);
+    MOE_STAMP(2);
     if (ok) {
         if (bad && threadIdx.x == 0) raise_error(a.err, MOE_ERR_TOPK_OUT_OF_RANGE);
         phase_tables(a, region);
-        ok = grid_barrier(a.barrier, 2 * n, a.err);
+        MOE_STAMP(3);
+        ok = grid_barrier(a.barrier, 2 * n, a.err, a.spin_limit, false);
+        MOE_STAMP(4);
     }
     if (!ok) {
         if (lane == 0) ring_drain(a, ring, 0);
+        MOE_PROF_END();
         return;
     }
     phase_payload(a, ring, prb);
+    MOE_STAMP(5);
+    MOE_PROF_END();
 }
+
+// The next moe_dispatch_fused call of this host thread, when armed by
+// moe_test_fused_barrier: grid-barrier spin limit and the CTA that leaves out
+// its first arrival.
+thread_local uint32_t t_test_spin_limit = 0;
+thread_local int64_t t_test_skip_cta = -1;
 
 // Row buffers per warp, the offset of the phase A / B region and the dynamic
 // shared memory of the launch, for a budget of `limit` bytes.
@@ -579,6 +599,11 @@ void fused_plan(const moe_shape& s, int64_t limit, int* nb, uint32_t* ab_off, si
 }
 
 }  // namespace
+
+void arm_fused_barrier_test(uint32_t spin_limit, int64_t skip_cta) {
+    t_test_spin_limit = spin_limit;
+    t_test_skip_cta = skip_cta;
+}
 
 bool fused_supported(const moe_shape& s) {
     if (!(s.P <= kMaxP && s.E <= kMaxE && s.H <= kMaxH && s.K <= kMaxK && s.quant == 0 &&
@@ -636,6 +661,14 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
     a.ccT = reinterpret_cast<int32_t*>(sc + 256);
     a.ecount = a.ccT + a.PCp * s.P;
     a.err = err;
+    a.spin_limit = kSpinLimit;
+    a.skip_arrival = -1;
+    if (t_test_spin_limit != 0) {  // one call armed by moe_test_fused_barrier
+        a.spin_limit = t_test_spin_limit;
+        a.skip_arrival = t_test_skip_cta;
+        t_test_spin_limit = 0;
+        t_test_skip_cta = -1;
+    }
     const int static_smem = kernel_static_smem(reinterpret_cast<const void*>(fused_kernel));
     if (static_smem < 0) return cudaErrorInvalidDeviceFunction;
     int64_t limit = static_cast<int64_t>(device_optin_smem()) - static_smem;
@@ -688,8 +721,11 @@ cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* t
             if (slot) g_coop_pdl[dev].store(1, std::memory_order_relaxed);
             return e;
         }
-        if (known == 1) return e;  // it worked before: a real error
-        (void)cudaGetLastError();
+        // Only a refusal of the attribute combination itself is remembered;
+        // any other failure (e.g. too large for the SMs free right now, or an
+        // error left by earlier work) is returned, and the next call tries again.
+        if (known == 1 || (e != cudaErrorNotSupported && e != cudaErrorInvalidValue)) return e;
+        (void)cudaGetLastError();  // clears this launch's own refusal
         if (slot) g_coop_pdl[dev].store(2, std::memory_order_relaxed);
     }
     cfg.numAttrs = 1;

@@ -154,8 +154,8 @@ __host__ __device__ __forceinline__ void split_range(int64_t n, int64_t b, int64
 // MOE_PROF_BEGIN, slot p = clock64 cycles from MOE_PROF_BEGIN to the end of
 // phase p (0 if not reached). CTAs at or beyond kProfCtas record nothing.
 // Loop phases that repeat inside a CTA (the int8 consumer's per-token steps)
-// instead add their cycles into a slot (MOE_PROF_ADD), summed by the CTA's
-// first consumer warp.
+// are summed in registers by one thread and written with MOE_PROF_PUT, the
+// start stamp alone then being published with MOE_PROF_END_N(1).
 #ifdef MOE_PROFILE
 constexpr int kProfKernels = MOE_PROF_KERNELS;
 constexpr int kProfCtas = MOE_PROF_CTAS;
@@ -188,14 +188,16 @@ __device__ __forceinline__ unsigned long long* prof_row(int kernel) {
         if (threadIdx.x == 0)                                                         \
             moe_prof_sm_[(phase)] = static_cast<unsigned long long>(clock64() - moe_prof_c0_); \
     } while (0)
-#define MOE_PROF_END()                                                                \
+#define MOE_PROF_END_N(n)                                                             \
     do {                                                                              \
         if (moe_prof_row_ && threadIdx.x == 0)                                        \
-            for (int moe_i_ = 0; moe_i_ < kProfPhases; ++moe_i_) moe_prof_row_[moe_i_] = moe_prof_sm_[moe_i_]; \
+            for (int moe_i_ = 0; moe_i_ < (n); ++moe_i_) moe_prof_row_[moe_i_] = moe_prof_sm_[moe_i_]; \
     } while (0)
-#define MOE_PROF_ADD(phase, cycles)                                                   \
+#define MOE_PROF_END() MOE_PROF_END_N(kProfPhases)
+#define MOE_PROF_CLOCK() clock64()
+#define MOE_PROF_PUT(phase, value)                                                    \
     do {                                                                              \
-        if (moe_prof_row_) moe_prof_row_[(phase)] += (cycles);                        \
+        if (moe_prof_row_) moe_prof_row_[(phase)] = static_cast<unsigned long long>(value); \
     } while (0)
 // Defines prof_attach_<unit>(), which points this unit's kernels at `slots`.
 #define MOE_PROFILE_UNIT(unit)                                                      \
@@ -216,11 +218,15 @@ cudaError_t prof_attach_expert(void*);
 #define MOE_PROF_END() \
     do {               \
     } while (0)
+#define MOE_PROF_END_N(n) \
+    do {                  \
+    } while (0)
 #define MOE_STAMP(phase) \
     do {                 \
     } while (0)
-#define MOE_PROF_ADD(phase, cycles) \
-    do {                            \
+#define MOE_PROF_CLOCK() 0ll
+#define MOE_PROF_PUT(phase, value) \
+    do {                           \
     } while (0)
 #define MOE_PROFILE_UNIT(unit)
 #endif
@@ -299,6 +305,8 @@ cudaError_t launch_pad(const moe_shape& s, const int32_t* nrt, const int64_t* pr
                        cudaStream_t stream);
 
 bool fused_supported(const moe_shape& s);
+// Test hook behind moe_test_fused_barrier (this host thread's next fused launch).
+void arm_fused_barrier_test(uint32_t spin_limit, int64_t skip_cta);
 int64_t fused_scratch_bytes(const moe_shape& s);
 cudaError_t launch_fused(const moe_shape& s, const uint16_t* x, const int32_t* topk_idx, const float* topk_weights,
                          int32_t* ntpr, int32_t* ntpe, uint8_t* itr, uint32_t* bits, int32_t* rpm, int32_t* cpm,

@@ -30,7 +30,7 @@ EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scrat
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
            "moe_layout_static_scratch", "moe_pad_partitions", "moe_max_expert_rows",
            "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused",
-           "moe_run_host_workspace_bytes", "moe_run_host")
+           "moe_run_host_workspace_bytes", "moe_run_host", "moe_test_fused_barrier")
 
 # moe_run_host flags (include/moe.h).
 MOE_RUN_FUSED = 1
@@ -119,6 +119,8 @@ def _open_lib() -> ctypes.CDLL:
     L.moe_run_host_workspace_bytes.argtypes = [sp, i32]
     L.moe_run_host.restype = i32
     L.moe_run_host.argtypes = [sp, i32, vp, vp, vp, vp, vp, i64, i32, vp, i64, vp]
+    L.moe_test_fused_barrier.restype = i32
+    L.moe_test_fused_barrier.argtypes = [ctypes.c_uint32, i32]
     _lib = L
     return L
 
@@ -290,6 +292,13 @@ def _host_ptr(t):
     if not t.flags["C_CONTIGUOUS"]:
         raise ValueError("expected a contiguous array")
     return t.ctypes.data
+
+
+def moe_test_fused_barrier(spin_limit: int, skip_cta: int) -> None:
+    """Arm the next moe_dispatch_fused call of this thread with a short grid
+    barrier and (skip_cta >= 0) one CTA that leaves out its first arrival, so
+    that its bounded waits run out (a test of the timeout path)."""
+    _check(lib().moe_test_fused_barrier(int(spin_limit), int(skip_cta)), "moe_test_fused_barrier")
 
 
 def moe_run_host_workspace_bytes(shape: moe_shape, n_batches: int) -> int:

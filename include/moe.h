@@ -414,6 +414,20 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
                         void* workspace, int64_t workspace_bytes, int32_t* err_host);
 
 /*
+ * moe_test_fused_barrier -- test hook for the bounded waits of
+ * moe_dispatch_fused; the pages have no counterpart. It arms the NEXT
+ * moe_dispatch_fused call made by this host thread (and that call only):
+ * each of its grid barriers gives up after `spin_limit` polls (instead of
+ * several million), and if skip_cta >= 0 the CTA with that index leaves out
+ * its arrival at the first barrier. Every CTA's wait then runs out: the call
+ * records MOE_ERR_DEVICE_TIMEOUT in err, each CTA waits (bounded) for its own
+ * row loads to land and returns, and the context stays usable. It exists so
+ * that tests can make a device-side wait time out without a fault. Returns
+ * MOE_ERR_INVALID_ARG for spin_limit = 0.
+ */
+moe_status moe_test_fused_barrier(uint32_t spin_limit, int32_t skip_cta);
+
+/*
  * moe_profile_attach -- profile builds only (compiled with -DMOE_PROFILE into
  * libmoe_profile.so; the default libmoe.so has no such symbol and its kernels
  * record nothing). The pages' "Ascend DeepEP MoE Dispatch Optimization",

@@ -132,3 +132,38 @@ def test_fused_no_tokens():
     for t in (buf.num_tokens_per_rank, buf.num_tokens_per_expert, buf.rank_prefix_matrix,
               buf.num_recv_tokens, buf.num_recv_tokens_per_expert, buf.recv_expert_offset, buf.part_row_base):
         assert (t.cpu().numpy() == 0).all()
+
+
+def test_fused_grid_barrier_times_out_and_the_context_stays_usable():
+    """The fused launch's bounded grid barrier, made to run out: with the test
+    hook one CTA leaves out its arrival and the barrier gives up after 10^4
+    polls. Every CTA records MOE_ERR_DEVICE_TIMEOUT, drains its own row loads
+    and returns (no trap, no fault, nothing left waiting); a normal fused call
+    on the same stream right after is bit-exact with the oracle."""
+    import time
+
+    import torch
+
+    w = inputs.workload("p32_e256_t128_h1024", T=32)
+    dev = torch.device("cuda", 0)
+    shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0)
+    buf = moe.Buffers(shape, dev)
+    x = torch.from_numpy(w.x_bits.view(np.int16)).to(dev)
+    idx = torch.from_numpy(w.topk_idx).to(dev)
+    wts = torch.from_numpy(w.topk_weights).to(dev)
+    for skip in (0, 5):
+        buf.err.fill_(0)
+        moe.moe_test_fused_barrier(10_000, skip)
+        t0 = time.perf_counter()
+        buf.dispatch_fused(x, idx, wts)
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 10.0
+        assert int(buf.err[0].item()) == moe.MOE_ERR_DEVICE_TIMEOUT
+    # the hook armed one call only: this one runs normally
+    gpu = _check_fused(w)
+    assert gpu["err"] == 0
+
+
+def test_fused_test_hook_rejects_a_zero_limit():
+    with pytest.raises(moe.MoeError):
+        moe.moe_test_fused_barrier(0, 0)
