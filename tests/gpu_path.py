@@ -34,8 +34,12 @@ def expert_stage_int8(arena, recv_topk_idx, rows, H):
     return y.to(torch.bfloat16).view(torch.int16).contiguous()
 
 
+CANARY = 0xA5       # arena bytes before dispatch (canary runs)
+SIDE_CANARY = -7    # side-array entries before dispatch
+
+
 def run_gpu(w, quant=0, weights=True, arena_rows=None, part_row_base=None, y_mode="identity",
-            topk_idx=None, repeat=1):
+            topk_idx=None, repeat=1, canary=False, guard_rows=0):
     """Run layout -> notify -> dispatch -> combine on cuda:0; return numpy outputs.
 
     part_row_base (host int64 [P+1]) replaces notify's packed bases before
@@ -43,13 +47,18 @@ def run_gpu(w, quant=0, weights=True, arena_rows=None, part_row_base=None, y_mod
     dispatch arena), "int8expert" (the stand-in expert above), "random"
     (fresh bf16 rows in a compact [rows, H] tensor), "allbf16" (every finite
     bf16 value, in a seeded order) or "fill:0x...." (one bf16 bit pattern).
+    canary: the arena is filled with CANARY bytes (not zeros) before dispatch,
+    so check_canaries can find stray writes. guard_rows: that many rows are
+    allocated past the arena_rows the calls are given.
     """
     import torch
 
     dev = torch.device("cuda", 0)
     idx_np = w.topk_idx if topk_idx is None else topk_idx
     shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, quant)
-    buf = moe.Buffers(shape, dev, arena_rows=arena_rows)
+    rows_given = moe.moe_max_recv_rows(shape) if arena_rows is None else arena_rows
+    buf = moe.Buffers(shape, dev, arena_rows=rows_given + guard_rows)
+    buf.arena_rows = rows_given  # the calls see only these rows; the guard rows follow
     x = torch.from_numpy(w.x_bits.view(np.int16)).to(dev)
     idx = torch.from_numpy(np.ascontiguousarray(idx_np, np.int32)).to(dev)
     wts = torch.from_numpy(w.topk_weights).to(dev)
@@ -63,10 +72,13 @@ def run_gpu(w, quant=0, weights=True, arena_rows=None, part_row_base=None, y_mod
         buf.notify()
         if part_row_base is not None:
             buf.part_row_base.copy_(torch.from_numpy(np.asarray(part_row_base, np.int64)))
-        buf.recv_arena.zero_()
-        buf.recv_src_idx.fill_(-7)
-        buf.recv_topk_idx.fill_(-7)
-        buf.recv_topk_weights.fill_(-7.0)
+        if canary:
+            buf.recv_arena.fill_(CANARY)
+        else:
+            buf.recv_arena.zero_()
+        buf.recv_src_idx.fill_(SIDE_CANARY)
+        buf.recv_topk_idx.fill_(SIDE_CANARY)
+        buf.recv_topk_weights.fill_(float(SIDE_CANARY))
         buf.dispatch(x, idx, wts)
         torch.cuda.synchronize()
         res["dispatch_err"] = int(buf.err[0].item())
@@ -226,3 +238,38 @@ def compare_combine(w, gpu, nt, tokens=None, weights=True):
     dist = bf16_ulp_distance(got, want)
     assert dist.max() <= 1, f"combine beyond 1 bf16 ulp: max {dist.max()}"
     np.testing.assert_array_equal(got, want, err_msg="combine bits")
+
+
+def check_canaries(gpu, quant, H, written_rows):
+    """Stray-write check after a canary run (run_gpu(..., canary=True)): in
+    every written row each byte outside the fields the slot format defines
+    (payload; the scale block, int8 only; the triple block) still holds the
+    canary, the defined blocks' padding is zero, and every other row of the
+    allocation -- guard rows past arena_rows included -- and every side-array
+    entry of an unwritten row still hold their canaries. Element-wise, on the
+    device."""
+    import torch
+
+    buf = gpu["buf"]
+    A = buf.recv_arena
+    dev = A.device
+    n_alloc = A.shape[0]
+    pay, scale_off, triple_off = offsets(H, quant)
+    written = torch.zeros(n_alloc, dtype=torch.bool, device=dev)
+    if len(written_rows):
+        written[torch.as_tensor(np.asarray(written_rows, np.int64), device=dev)] = True
+    Wr = A[written]
+    c = CANARY
+    assert bool((Wr[:, pay:scale_off] == c).all()), "bytes between the payload and the scale block"
+    if quant:
+        assert bool((Wr[:, scale_off + 4:scale_off + 32] == 0).all()), "scale block padding"
+    else:
+        assert bool((Wr[:, scale_off:scale_off + 32] == c).all()), "bf16 slots leave the scale block alone"
+    assert bool((Wr[:, triple_off + 12:triple_off + 32] == 0).all()), "triple block padding"
+    assert bool((Wr[:, triple_off + 32:] == c).all()), "slot padding after the triple block"
+    assert bool((A[~written] == c).all()), "rows nothing was sent to"
+    for name in ("recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        t = getattr(buf, name)
+        if t is None:
+            continue
+        assert bool((t[~written] == SIDE_CANARY).all()), name

@@ -15,10 +15,15 @@ pytestmark = pytest.mark.gpu
 
 
 def _check_all(w, quant=0, weights=True, y_mode="identity", sample=None, seed=0):
-    gpu = gp.run_gpu(w, quant=quant, weights=weights, y_mode=y_mode)
+    """Every table in full; dispatch and combine for all tokens (or a sample);
+    and, the arena having been filled with canaries, no byte written outside
+    the slot fields of the rows the routing sends (guard rows past the arena
+    included)."""
+    gpu = gp.run_gpu(w, quant=quant, weights=weights, y_mode=y_mode, canary=True, guard_rows=3)
     lay, nt = gp.oracle_tables(w)
     assert gpu["layout_err"] == 0 and gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
     gp.assert_tables_equal(gpu, lay, nt)
+    gp.check_canaries(gpu, quant, w.H, np.arange(int(nt["part_row_base"][-1])))
     tokens = None
     if sample is not None and sample < w.S:
         rng = np.random.default_rng(seed)
@@ -122,21 +127,29 @@ def test_fixed_capacity_partitions():
     lay, nt = gp.oracle_tables(w)
     cap = int(nt["num_recv_tokens"].max())
     prb = np.arange(w.P + 1, dtype=np.int64) * cap
-    gpu = gp.run_gpu(w, arena_rows=cap * w.P, part_row_base=prb)
+    gpu = gp.run_gpu(w, arena_rows=cap * w.P, part_row_base=prb, canary=True, guard_rows=4)
     assert gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
-    gp.compare_dispatch(w, 0, gpu, nt, part_row_base=prb)
+    _, rows = gp.compare_dispatch(w, 0, gpu, nt, part_row_base=prb)
+    gp.check_canaries(gpu, 0, w.H, rows)  # the gaps at the partitions' ends stay untouched
     nt_cap = dict(nt, part_row_base=prb)
     gp.compare_combine(w, gpu, nt_cap)
 
 
-def test_capacity_overflow_reported_without_stray_writes():
+@pytest.mark.parametrize("quant", [0, 1])
+def test_capacity_overflow_reported_without_stray_writes(quant):
+    """Partitions too small for their rows: the overflow is reported, the rows
+    that fit are exact, and no byte is written anywhere else -- not in the
+    padding of written slots, not in rows past a partition's rows, not in
+    the guard rows allocated past the arena the call was given."""
     w = inputs.make(4, 16, 64, 128, 2, seed=10)
     lay, nt = gp.oracle_tables(w)
     cap = int(nt["num_recv_tokens"].min()) - 2
     prb = np.arange(w.P + 1, dtype=np.int64) * cap
-    gpu = gp.run_gpu(w, arena_rows=cap * w.P, part_row_base=prb)
+    gpu = gp.run_gpu(w, quant=quant, arena_rows=cap * w.P, part_row_base=prb, canary=True, guard_rows=5,
+                     y_mode="int8expert" if quant else "identity")
     assert gpu["dispatch_err"] == moe.MOE_ERR_CAPACITY
-    gp.compare_dispatch(w, 0, gpu, nt, part_row_base=prb)
+    _, rows = gp.compare_dispatch(w, quant, gpu, nt, part_row_base=prb)
+    gp.check_canaries(gpu, quant, w.H, rows)
 
 
 def test_deterministic_repeat():
@@ -214,18 +227,52 @@ def test_combine_column_halves_with_odd_chunk_count():
     ("p32_e256_t128_h7168", 0, "identity"),
     ("p32_e256_t128_h1024", 0, "identity"),
 ])
-def test_full_size_sampled(name, quant, y_mode):
+def test_full_size_every_row(name, quant, y_mode):
+    """The bench's workloads at full size, in the bench's launch configuration:
+    every table, every received row (payload, scale, triple, side arrays) and
+    every combined token compared with the oracle element by element, and the
+    canary check over the whole arena."""
+    import torch
+
+    import oracle
+
     w = inputs.workload(name)
-    gpu, lay, nt = _check_all(w, quant=quant, y_mode=y_mode, sample=1500)
-    # Whole-array properties at full size.
-    assert gpu["part_row_base"][-1] == gpu["is_token_in_rank"].sum()
+    gpu = gp.run_gpu(w, quant=quant, y_mode=y_mode, canary=True, guard_rows=2)
+    assert gpu["layout_err"] == 0 and gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
+    lay, nt = gp.oracle_tables(w)
+    gp.assert_tables_equal(gpu, lay, nt)
+    buf = gpu["buf"]
+    R = int(nt["part_row_base"][-1])
+    assert R == int(lay["is_token_in_rank"].sum())
+    ref = oracle.dispatch(w.P, w.E, w.H, quant, w.x_bits, w.topk_idx, w.topk_weights, nt["send_head"],
+                          nt["part_row_base"], R)
+    assert ref["err"] == 0
+    pay, scale_off, triple_off = gp.offsets(w.H, quant)
+    got = buf.recv_arena[:R].cpu().numpy()
+    np.testing.assert_array_equal(got[:, :pay], ref["arena"][:, :pay], err_msg="payload")
+    np.testing.assert_array_equal(got[:, triple_off:triple_off + 12], ref["arena"][:, triple_off:triple_off + 12],
+                                  err_msg="triple")
+    if quant:
+        np.testing.assert_array_equal(got[:, scale_off:scale_off + 4], ref["arena"][:, scale_off:scale_off + 4],
+                                      err_msg="scale")
+    for k in ("recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        np.testing.assert_array_equal(getattr(buf, k)[:R].cpu().numpy(), ref[k][:R], err_msg=k)
+    del got
+    gp.check_canaries(gpu, quant, w.H, np.arange(R))
+    # Combine over every token, on the y rows the GPU combine read.
     if y_mode == "identity":
-        # Softmax weights with identity experts return x (ties of -0 become +0).
+        y, y_stride = ref["arena"], buf.stride  # equal to the GPU arena in every byte combine reads
+    else:
+        y, y_stride = gpu["y"][:R].cpu().numpy().view(np.uint8), 2 * w.H
+    comb = oracle.combine(w.P, w.E, w.H, np.ascontiguousarray(y), y_stride, nt["part_row_base"], R,
+                          nt["send_head"], w.topk_idx, w.topk_weights)
+    np.testing.assert_array_equal(gpu["out"], comb["out"], err_msg="combine")
+    if y_mode == "identity" and not (w.topk_idx < 0).any():
+        # softmax weights with identity experts give x back within 1 ulp
         from tests.helpers import bf16_ulp_distance
-        d = bf16_ulp_distance(gpu["out"], w.x_bits)
-        masked_any = (w.topk_idx < 0).any()
-        if not masked_any:
-            assert d.max() <= 1
+        assert bf16_ulp_distance(gpu["out"], w.x_bits).max() <= 1
+    del ref, comb
+    torch.cuda.empty_cache()
 
 
 def test_cached_dispatch_reuses_the_handle():
