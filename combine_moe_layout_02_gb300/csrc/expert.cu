@@ -10,182 +10,192 @@
 //   slot_row[g][k] = recv_expert_offset[e] + #(slots of expert e before (g, k))
 //   expert_part_base[d] = sum over d' < d of sum_l num_recv_tokens_per_expert[d'][l]
 //
-// Three launches over "chunks" of kChunkTokens consecutive tokens. A chunk's
-// slots are contiguous in topk_idx ([S, K] row-major), so one warp loads all
-// of them at once, 32 consecutive slots per step, lanes in (token, k) order.
-//  1. count: per-chunk expert histograms (shared-memory integer atomics) into
-//     scratch, expert-major: ecount[e][chunk];
-//  2. scan: one warp per expert turns its contiguous column into the chunks'
-//     first rows (16-byte loads, one warp scan per 512 chunks), starting at
-//     recv_expert_offset, written chunk-major: ebase[chunk][e]; one more warp
-//     scans the rank totals into expert_part_base;
-//  3. rows: each chunk's warp starts its counters at those bases and ranks
-//     every slot among the step's slots of the same expert
-//     (__match_any_sync), in (token, k) order.
+// Two launches over chunks of kChunk consecutive tokens, one CTA per chunk
+// and one thread per token (a token's K slots are contiguous in topk_idx):
+//  1. count: the chunk's expert histogram (shared-memory integer atomics)
+//     into scratch, expert-major: ecount[e][chunk];
+//  2. rows: each CTA adds, per expert, the counts of the chunks before its own
+//     (its row of ecount, 16-byte loads) to recv_expert_offset -- the chunk's
+//     first row of every expert; per-warp histograms of the chunk become
+//     exclusive warp offsets; then each warp ranks its slots 32 at a time in
+//     (token, k) order among the step's slots of the same expert
+//     (__match_any_sync). CTA 0 also scans the rank totals into
+//     expert_part_base.
 // Integer counts: the result does not depend on the order of the atomics.
 #include "moe_device.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kChunkTokens = 32;
-constexpr int kThreads = 256;
-constexpr int kMaxSteps = kChunkTokens * 16 / 32;  // slots per chunk / 32, for K <= 16
-constexpr int kSeg = 16;                            // chunks per lane per scan block
+constexpr int kChunk = 1024;   // tokens per chunk = threads per CTA
+constexpr int kWarps = kChunk / 32;
 
 struct ExpertPlan {
-    int64_t chunks, chunks_pad;  // chunk count; expert-major row stride (multiple of 4)
-    int wpb;                     // warps (chunks) per block, bounded by E counters in shared memory
-    int64_t blocks;              // blocks of the chunk kernels
-    size_t smem;                 // wpb * E * 4
-    int64_t ebase_off, scratch_bytes;
+    int64_t chunks, chunks_pad;  // chunk count; expert-major row stride (a multiple of 4)
+    int threads;                 // kChunk, or fewer (a multiple of 32) when S is smaller
+    size_t smem_count, smem_rows;
+    int64_t scratch_bytes;
 };
 
 ExpertPlan expert_plan(const moe_shape& s) {
     ExpertPlan p;
-    p.chunks = ceil_div(s.S, kChunkTokens);
+    // One token per thread and about 64 chunks (measured best at S = 4096,
+    // 32768 and 65536: fewer chunks leave SMs idle, more lengthen each CTA's
+    // prefix over the earlier chunks): a power of two from 256 to kChunk, no
+    // more than S needs, and few enough warps that their histograms
+    // ([warps][E]) stay within 128 KB.
+    int64_t t = 256;
+    while (t < kChunk && t * 64 < s.S) t <<= 1;
+    if (t > s.S) t = round_up(s.S > 0 ? s.S : 1, 32);
+    const int64_t by_smem = (128 * 1024 / (static_cast<int64_t>(s.E) * 4)) / 1 * 32;
+    if (t > by_smem) t = by_smem < 32 ? 32 : by_smem / 32 * 32;
+    p.threads = static_cast<int>(t);
+    p.chunks = ceil_div(s.S, t);
     p.chunks_pad = round_up(p.chunks, 4);
-    int wpb = static_cast<int>((64 * 1024) / (static_cast<int64_t>(s.E) * 4));
-    p.wpb = wpb < 1 ? 1 : (wpb > kThreads / 32 ? kThreads / 32 : wpb);
-    p.blocks = ceil_div(p.chunks, p.wpb);
-    p.smem = static_cast<size_t>(p.wpb) * s.E * 4;
-    p.ebase_off = round_up(static_cast<int64_t>(s.E) * p.chunks_pad * 4, 256);
-    p.scratch_bytes = p.ebase_off + round_up(p.chunks * s.E * 4, 256);
+    p.smem_count = static_cast<size_t>(s.E) * 4;
+    // per-warp histograms [warps][E], the chunk's bases [E] and slot ids [threads][K]
+    p.smem_rows = (static_cast<size_t>(p.threads / 32) + 1) * s.E * 4 + static_cast<size_t>(p.threads) * s.K * 4;
+    p.scratch_bytes = round_up(static_cast<int64_t>(s.E) * p.chunks_pad * 4, 256);
     return p;
 }
 
-// The chunk's slots, 32 per step: lane `lane` of step st holds slot
-// f = 32 * st + lane of the chunk ((token, k) order), or -1 beyond the chunk
-// or for a masked / out-of-range id.
-__device__ __forceinline__ void load_chunk(const int32_t* __restrict__ topk_idx, int64_t f0, int nslots, int E,
-                                           int lane, int32_t (&ids)[kMaxSteps]) {
+// Token g's K expert ids (out-of-range and masked ids as -1), 16-byte loads
+// when K is a multiple of 4.
+__device__ __forceinline__ void load_ids(const int32_t* __restrict__ topk_idx, int64_t g, bool active, int K, int E,
+                                         int32_t (&ids)[MOE_MAX_TOPK]) {
+    if ((K & 3) == 0) {
 #pragma unroll
-    for (int st = 0; st < kMaxSteps; ++st) {
-        const int f = st * 32 + lane;
-        int32_t e = -1;
-        if (f < nslots) {
-            e = __ldg(topk_idx + f0 + f);
-            if (e < 0 || e >= E) e = -1;
+        for (int k4 = 0; k4 < MOE_MAX_TOPK; k4 += 4) {
+            if (k4 < K) {
+                const int4 v = active ? __ldg(reinterpret_cast<const int4*>(topk_idx + g * K + k4))
+                                      : make_int4(-1, -1, -1, -1);
+                ids[k4] = v.x;
+                ids[k4 + 1] = v.y;
+                ids[k4 + 2] = v.z;
+                ids[k4 + 3] = v.w;
+            }
         }
-        ids[st] = e;
+    } else {
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; ++k)
+            if (k < K) ids[k] = active ? __ldg(topk_idx + g * K + k) : -1;
     }
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k)
+        if (k < K && (ids[k] < 0 || ids[k] >= E)) ids[k] = -1;
 }
 
-__global__ void __launch_bounds__(kThreads)
-expert_count_kernel(int32_t E, int32_t K, int64_t S, int64_t chunks, int64_t chunks_pad,
-                    const int32_t* __restrict__ topk_idx, int32_t* __restrict__ ecount) {
+__global__ void __launch_bounds__(kChunk)
+expert_count_kernel(int32_t E, int32_t K, int64_t S, int64_t chunks_pad, const int32_t* __restrict__ topk_idx,
+                    int32_t* __restrict__ ecount) {
     pdl_wait_then_release();
-    extern __shared__ __align__(16) int32_t hist_all[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
-    if (chunk >= chunks) return;
-    int32_t* hist = hist_all + warp * E;
-    const int64_t g0 = chunk * kChunkTokens;
-    const int64_t g1 = g0 + kChunkTokens < S ? g0 + kChunkTokens : S;
-    const int nslots = static_cast<int>((g1 - g0) * K);
-    int32_t ids[kMaxSteps];
-    load_chunk(topk_idx, g0 * K, nslots, E, lane, ids);
-    for (int e = lane; e < E; e += 32) hist[e] = 0;
-    __syncwarp();
+    extern __shared__ __align__(16) int32_t hist[];  // [E]
+    const int tid = threadIdx.x;
+    const int64_t chunk = blockIdx.x;
+    const int64_t g = chunk * blockDim.x + tid;
+    int32_t ids[MOE_MAX_TOPK];
+    load_ids(topk_idx, g, g < S, K, E, ids);
+    for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
 #pragma unroll
-    for (int st = 0; st < kMaxSteps; ++st)
-        if (ids[st] >= 0) atomicAdd(hist + ids[st], 1);
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) ecount[static_cast<int64_t>(e) * chunks_pad + chunk] = hist[e];
+    for (int k = 0; k < MOE_MAX_TOPK; ++k)
+        if (k < K && ids[k] >= 0) atomicAdd(hist + ids[k], 1);
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) ecount[static_cast<int64_t>(e) * chunks_pad + chunk] = hist[e];
 }
 
-__global__ void __launch_bounds__(kThreads)
-expert_scan_kernel(int32_t P, int32_t E, int64_t chunks, int64_t chunks_pad, const int32_t* __restrict__ reo,
-                   const int32_t* __restrict__ nrtpe, const int32_t* __restrict__ ecount,
-                   int32_t* __restrict__ ebase, int64_t* __restrict__ expert_part_base) {
+__global__ void __launch_bounds__(kChunk)
+expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, int64_t chunks_pad,
+                   const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ ecount,
+                   const int32_t* __restrict__ reo, const int32_t* __restrict__ nrtpe, int32_t* __restrict__ slot_row,
+                   int64_t* __restrict__ expert_part_base) {
     pdl_wait_then_release();
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (gw < E) {
-        const int64_t e = gw;
-        const int32_t* col = ecount + e * chunks_pad;
-        int32_t carry = __ldg(reo + e);
-        for (int64_t c0 = 0; c0 < chunks; c0 += 32 * kSeg) {
-            const int64_t cb = c0 + static_cast<int64_t>(lane) * kSeg;
-            int32_t v[kSeg];
+    extern __shared__ __align__(16) int32_t sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int32_t* whist = sm;                       // [nwarps][E]: counts, then each warp's first rows
+    int32_t* cbase = sm + nwarps * E;          // [E]: the chunk's first row of each expert
+    int32_t* sids = cbase + E;                 // [threads][K]: the chunk's slot ids in (token, k) order
+    const int64_t chunk = blockIdx.x;
+    const int64_t g0 = chunk * blockDim.x;
+    const bool work = chunk < chunks;
+
+    if (chunk == 0) {  // the expert-major partition bases, from the aligned counts
+        if (warp == nwarps - 1) {
+            const int epr = E / P;
+            int64_t run = 0;
+            for (int d0 = 0; d0 < P; d0 += 32) {
+                const int d = d0 + lane;
+                int64_t v = 0;
+                if (d < P)
+                    for (int l = 0; l < epr; ++l) v += __ldg(nrtpe + static_cast<int64_t>(d) * epr + l);
+                int64_t incl = v;
 #pragma unroll
-            for (int q = 0; q < kSeg; q += 4) {
-                // cb + q is a multiple of 4 and so is the row stride: whole int4 inside the row
-                const int4 u = cb + q < chunks_pad ? __ldg(reinterpret_cast<const int4*>(col + cb + q))
-                                                   : make_int4(0, 0, 0, 0);
-                v[q] = u.x;
-                v[q + 1] = u.y;
-                v[q + 2] = u.z;
-                v[q + 3] = u.w;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += u;
+                }
+                if (d < P) expert_part_base[d] = run + incl - v;
+                run += __shfl_sync(0xffffffffu, incl, 31);
             }
-            int32_t sum = 0;
-#pragma unroll
-            for (int u = 0; u < kSeg; ++u) {
-                if (cb + u >= chunks) v[u] = 0;  // row padding
-                sum += v[u];
-            }
-            int32_t incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            int32_t run = carry + incl - sum;
-#pragma unroll
-            for (int u = 0; u < kSeg; ++u) {
-                if (cb + u < chunks) ebase[(cb + u) * E + e] = run;
-                run += v[u];
-            }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
+            if (lane == 0) expert_part_base[P] = run;
         }
-    } else if (gw == E) {
-        const int epr = E / P;
-        int64_t run = 0;
-        for (int d0 = 0; d0 < P; d0 += 32) {
-            const int d = d0 + lane;
-            int64_t v = 0;
-            if (d < P)
-                for (int l = 0; l < epr; ++l) v += __ldg(nrtpe + static_cast<int64_t>(d) * epr + l);
-            int64_t incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            if (d < P) expert_part_base[d] = run + incl - v;
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) expert_part_base[P] = run;
     }
-}
+    if (!work) return;
 
-__global__ void __launch_bounds__(kThreads)
-expert_rows_kernel(int32_t E, int32_t K, int64_t S, int64_t chunks, const int32_t* __restrict__ topk_idx,
-                   const int32_t* __restrict__ ebase, int32_t* __restrict__ slot_row) {
-    pdl_wait_then_release();
-    extern __shared__ __align__(16) int32_t hist_all[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
-    if (chunk >= chunks) return;
-    int32_t* next = hist_all + warp * E;
-    const int64_t g0 = chunk * kChunkTokens;
-    const int64_t g1 = g0 + kChunkTokens < S ? g0 + kChunkTokens : S;
-    const int nslots = static_cast<int>((g1 - g0) * K);
-    int32_t ids[kMaxSteps];
-    load_chunk(topk_idx, g0 * K, nslots, E, lane, ids);
-    for (int e = lane; e < E; e += 32) next[e] = __ldg(ebase + chunk * E + e);
-    __syncwarp();
+    const int64_t g = g0 + tid;
+    int32_t ids[MOE_MAX_TOPK];
+    load_ids(topk_idx, g, g < S, K, E, ids);
+    // Chunk base of each expert: its first receive row plus the slots of the
+    // earlier chunks (this CTA's prefix of the expert's ecount row).
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t acc = __ldg(reo + e);
+        const int32_t* row = ecount + static_cast<int64_t>(e) * chunks_pad;
+        int64_t c = 0;
+#pragma unroll 4
+        for (; c + 4 <= chunk; c += 4) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(row + c));
+            acc += v.x + v.y + v.z + v.w;
+        }
+        for (; c < chunk; ++c) acc += __ldg(row + c);
+        cbase[e] = acc;
+    }
+    for (int i = tid; i < nwarps * E; i += blockDim.x) whist[i] = 0;
+    int32_t* srow = sids + tid * K;
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k)
+        if (k < K) srow[k] = ids[k];
+    __syncthreads();
+    int32_t* my = whist + warp * E;
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k)
+        if (k < K && ids[k] >= 0) atomicAdd(my + ids[k], 1);
+    __syncthreads();
+    // Exclusive warp offsets per expert, from the chunk base.
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t run = cbase[e];
+        for (int w = 0; w < nwarps; ++w) {
+            const int32_t v = whist[w * E + e];
+            whist[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    // Rank each slot among the earlier slots of its expert, 32 slots a step.
+    const int64_t wg0 = g0 + warp * 32;  // the warp's first token
+    const int ntok = static_cast<int>(min(static_cast<int64_t>(32), S - wg0));
+    if (ntok <= 0) return;
+    const int nslots = ntok * K;
+    const int32_t* wids = sids + warp * 32 * K;
+    int32_t* out = slot_row + wg0 * K;
     const uint32_t below = lanemask_lt();
-    int32_t* out = slot_row + g0 * K;
-#pragma unroll
-    for (int st = 0; st < kMaxSteps; ++st) {
-        if (st * 32 >= nslots) break;  // warp-uniform
-        const int f = st * 32 + lane;
-        const int32_t e = ids[st];
+    for (int f0 = 0; f0 < nslots; f0 += 32) {
+        const int f = f0 + lane;
+        const int32_t e = f < nslots ? wids[f] : -1;
         const uint32_t grp = __match_any_sync(0xffffffffu, e);
-        if (f < nslots) out[f] = e >= 0 ? next[e] + __popc(grp & below) : -1;
+        if (f < nslots) out[f] = e >= 0 ? my[e] + __popc(grp & below) : -1;
         __syncwarp();
-        if (e >= 0 && lane == 31 - __clz(grp)) next[e] += __popc(grp);
+        if (e >= 0 && lane == 31 - __clz(grp)) my[e] += __popc(grp);
         __syncwarp();
     }
 }
@@ -199,24 +209,20 @@ cudaError_t launch_notify_expert(const moe_shape& s, const int32_t* topk_idx, co
                                  void* scratch, cudaStream_t stream) {
     const ExpertPlan p = expert_plan(s);
     int32_t* ecount = static_cast<int32_t*>(scratch);
-    int32_t* ebase = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) + p.ebase_off);
     cudaError_t e = cudaSuccess;
     if (p.chunks > 0) {
-        e = prepare_kernel(reinterpret_cast<const void*>(expert_count_kernel), p.smem, p.wpb * 32, nullptr);
+        e = prepare_kernel(reinterpret_cast<const void*>(expert_count_kernel), p.smem_count, p.threads, nullptr);
         if (e != cudaSuccess) return e;
-        e = prepare_kernel(reinterpret_cast<const void*>(expert_rows_kernel), p.smem, p.wpb * 32, nullptr);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(expert_count_kernel, static_cast<unsigned>(p.blocks), p.wpb * 32, p.smem, stream, s.E,
-                       s.K, static_cast<int64_t>(s.S), p.chunks, p.chunks_pad, topk_idx, ecount);
+        e = launch_pdl(expert_count_kernel, static_cast<unsigned>(p.chunks), p.threads, p.smem_count, stream, s.E,
+                       s.K, static_cast<int64_t>(s.S), p.chunks_pad, topk_idx, ecount);
         if (e != cudaSuccess) return e;
     }
-    const int64_t scan_warps = static_cast<int64_t>(s.E) + 1;
-    e = launch_pdl(expert_scan_kernel, static_cast<unsigned>(ceil_div(scan_warps, kThreads / 32)), kThreads, 0,
-                   stream, s.P, s.E, p.chunks, p.chunks_pad, reo, nrtpe, static_cast<const int32_t*>(ecount), ebase,
-                   expert_part_base);
-    if (e != cudaSuccess || p.chunks == 0) return e;
-    return launch_pdl(expert_rows_kernel, static_cast<unsigned>(p.blocks), p.wpb * 32, p.smem, stream, s.E, s.K,
-                      static_cast<int64_t>(s.S), p.chunks, topk_idx, static_cast<const int32_t*>(ebase), slot_row);
+    e = prepare_kernel(reinterpret_cast<const void*>(expert_rows_kernel), p.smem_rows, p.threads, nullptr);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(p.chunks > 0 ? p.chunks : 1);
+    return launch_pdl(expert_rows_kernel, grid, p.threads, p.smem_rows, stream, s.P, s.E, s.K,
+                      static_cast<int64_t>(s.S), p.chunks, p.chunks_pad, topk_idx,
+                      static_cast<const int32_t*>(ecount), reo, nrtpe, slot_row, expert_part_base);
 }
 
 MOE_PROFILE_UNIT(expert)
