@@ -27,7 +27,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "layout.cu", "notify.cu", "dispatch.cu", "combine.cu", "layout_static.cu", "pad.cu", "expert.cu", "fused.cu", "run.cu"]
+SOURCES = ["api.cu", "layout.cu", "notify.cu", "dispatch.cu", "combine.cu", "layout_static.cu", "pad.cu", "expert.cu", "fused.cu", "run.cu", "exchange.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 VARIANTS = {"match_hist": ["-DMOE_LAYOUT_MATCH_HIST"], "profile": ["-DMOE_PROFILE"]}
 

@@ -302,11 +302,16 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // q = rint(x / scale) with round-half-even, exactly as with IEEE division, for
-// finite x. The quotient is taken as t = x * r, r = 1 / scale rounded:
-// |t - x / scale| <= 127 * 2^-23 < 2^-15, so rounding t gives the same integer
-// unless t lies within 2^-15 of a half-integer; only then (or when r is not
-// finite) is the division done. |x / scale| <= 127 * (1 + 2^-23) < 127.5, so
-// q is already in [-127, 127] and needs no clamp.
+// finite x. Bound on the quotient: scale = amax / 127 rounded, with an error
+// of at most half an ulp -- relative 2^-24 for a normal scale, absolute 2^-150
+// for a subnormal one. A bf16 amax is at least 2^-133 (the smallest bf16
+// denormal), so scale >= amax / 127 - 127 * 2^-17 * (amax / 127) and
+// |x / scale| <= amax / scale <= 127 / (1 - 127 * 2^-17) < 127.13 < 127.5:
+// q is already in [-127, 127], and the clamp the definition states never acts.
+// The quotient is taken as t = x * r, r = 1 / scale rounded (two roundings of
+// relative 2^-24 each): |t - x / scale| <= 127.13 * 2^-23 < 2^-15, so rounding
+// t gives the same integer unless t lies within 2^-15 of a half-integer; only
+// then (or when r is not finite) is the division done.
 __device__ __forceinline__ int32_t quant_one(float x, float scale, float r, bool fast) {
     const float t = __fmul_rn(x, r);
     int32_t q = __float2int_rn(t);

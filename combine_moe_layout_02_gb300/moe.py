@@ -30,7 +30,7 @@ EXPORTS = ("moe_status_string", "moe_check_shape", "moe_slot_stride", "moe_scrat
            "moe_max_recv_rows", "moe_layout", "moe_notify", "moe_dispatch", "moe_combine",
            "moe_layout_static_scratch", "moe_pad_partitions", "moe_max_expert_rows",
            "moe_notify_expert", "moe_dispatch_expert", "moe_combine_expert", "moe_dispatch_fused",
-           "moe_run_host_workspace_bytes", "moe_run_host", "moe_test_fused_barrier")
+           "moe_run_host_workspace_bytes", "moe_run_host", "moe_test_fused_barrier", "moe_exchange_plan")
 
 # moe_run_host flags (include/moe.h).
 MOE_RUN_FUSED = 1
@@ -121,6 +121,8 @@ def _open_lib() -> ctypes.CDLL:
     L.moe_run_host.argtypes = [sp, i32, vp, vp, vp, vp, vp, i64, i32, vp, i64, vp]
     L.moe_test_fused_barrier.restype = i32
     L.moe_test_fused_barrier.argtypes = [ctypes.c_uint32, i32]
+    L.moe_exchange_plan.restype = i32
+    L.moe_exchange_plan.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -299,6 +301,56 @@ def moe_test_fused_barrier(spin_limit: int, skip_cta: int) -> None:
     barrier and (skip_cta >= 0) one CTA that leaves out its first arrival, so
     that its bounded waits run out (a test of the timeout path)."""
     _check(lib().moe_test_fused_barrier(int(spin_limit), int(skip_cta)), "moe_test_fused_barrier")
+
+
+def moe_exchange_plan(shape: moe_shape, self_rank: int, ntpr_all, ntpe_all) -> dict:
+    """What rank self_rank needs from every rank's gathered layout rows (host
+    numpy arrays ntpr_all [P,P], ntpe_all [P,E]); the C function computes it on
+    the host (include/moe.h)."""
+    import numpy as np
+
+    P, E = shape.P, shape.E
+    ntpr = np.ascontiguousarray(ntpr_all, np.int32)
+    ntpe = np.ascontiguousarray(ntpe_all, np.int32)
+    if ntpr.shape != (P, P) or ntpe.shape != (P, E):
+        raise ValueError("expected ntpr_all [P,P] and ntpe_all [P,E]")
+    out = dict(rank_prefix_matrix=np.empty((P, P), np.int32), num_recv_tokens=np.empty((P,), np.int32),
+               send_row_base=np.empty((P,), np.int64),
+               num_recv_tokens_per_expert=np.empty((E // P,), np.int32),
+               recv_expert_offset=np.empty((E // P,), np.int32), part_row_base=np.empty((P + 1,), np.int64))
+    h = lambda a: a.ctypes.data
+    _check(lib().moe_exchange_plan(ctypes.byref(shape), int(self_rank), h(ntpr), h(ntpe),
+                                   h(out["rank_prefix_matrix"]), h(out["num_recv_tokens"]), h(out["send_row_base"]),
+                                   h(out["num_recv_tokens_per_expert"]), h(out["recv_expert_offset"]),
+                                   h(out["part_row_base"])), "moe_exchange_plan")
+    return out
+
+
+def exchange_counts(shape: moe_shape, num_tokens_per_rank_row, num_tokens_per_expert_row, group=None) -> dict:
+    """The count exchange of a path spread over the ranks of a torch.distributed
+    group (one expert-parallel rank per process, group size = shape.P): this
+    rank's rows of num_tokens_per_rank [P] and num_tokens_per_expert [E] (from
+    moe_layout over its own tokens) are all-gathered in rank order, then
+    moe_exchange_plan gives this rank's plan. The gathered tables are returned
+    too (ntpr_all, ntpe_all)."""
+    import torch
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    if world != shape.P:
+        raise ValueError(f"group of {world} ranks for P = {shape.P}")
+    row = torch.cat([torch.as_tensor(num_tokens_per_rank_row).reshape(-1).to(torch.int32),
+                     torch.as_tensor(num_tokens_per_expert_row).reshape(-1).to(torch.int32)])
+    if row.numel() != shape.P + shape.E:
+        raise ValueError("expected rows of P and E counts")
+    parts = [torch.empty_like(row) for _ in range(world)]
+    dist.all_gather(parts, row.contiguous(), group=group)
+    table = torch.stack(parts).cpu().numpy()
+    ntpr_all, ntpe_all = table[:, :shape.P], table[:, shape.P:]
+    plan = moe_exchange_plan(shape, rank, ntpr_all, ntpe_all)
+    plan.update(ntpr_all=ntpr_all, ntpe_all=ntpe_all)
+    return plan
 
 
 def moe_run_host_workspace_bytes(shape: moe_shape, n_batches: int) -> int:

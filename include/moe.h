@@ -414,6 +414,34 @@ moe_status moe_run_host(const moe_shape* shape, int32_t n_batches, const uint16_
                         void* workspace, int64_t workspace_bytes, int32_t* err_host);
 
 /*
+ * moe_exchange_plan -- HOST function, for the path spread over P GPUs (one
+ * expert-parallel rank each). After every rank has run moe_layout on its own
+ * T tokens, the ranks all-gather their rows of num_tokens_per_rank and
+ * num_tokens_per_expert ("internode.cu", section 1 notify_dispatch: counts
+ * exchanged, then global prefix sums; "Ascend DeepEP MoE Dispatch
+ * Optimization", section "Notify 先交换数量和前缀"). From the gathered tables
+ * this computes what rank `self` needs before any row moves; every value is
+ * the one moe_notify computes from the full tables.
+ *
+ *   ntpr_all [P,P], ntpe_all [P,E]   int32, host: row s = rank s's layout row
+ *   rank_prefix_matrix [P,P]         int32, host (or NULL): inclusive column prefix
+ *   num_recv_tokens [P]              int32, host (or NULL): rows each rank receives
+ *   send_row_base [P]                int64, host (or NULL): first row of self's
+ *                                    tokens inside rank d's receive partition
+ *   self_recv_tokens_per_expert [E/P] int32, host (or NULL): self's experts'
+ *                                    receive counts, rounded up to expert_alignment
+ *   self_recv_expert_offset [E/P]    int32, host (or NULL): their exclusive scan
+ *   part_row_base [P+1]              int64, host (or NULL): the packed bases of all
+ *                                    partitions (the one-GPU emulation's layout)
+ * Touches no device. Returns MOE_ERR_INVALID_ARG for a bad rank or a negative
+ * count, MOE_ERR_UNSUPPORTED if a count overflows int32.
+ */
+moe_status moe_exchange_plan(const moe_shape* shape, int32_t self, const int32_t* ntpr_all,
+                             const int32_t* ntpe_all, int32_t* rank_prefix_matrix, int32_t* num_recv_tokens,
+                             int64_t* send_row_base, int32_t* self_recv_tokens_per_expert,
+                             int32_t* self_recv_expert_offset, int64_t* part_row_base);
+
+/*
  * moe_test_fused_barrier -- test hook for the bounded waits of
  * moe_dispatch_fused; the pages have no counterpart. It arms the NEXT
  * moe_dispatch_fused call made by this host thread (and that call only):
