@@ -613,9 +613,9 @@ def run_ours(args, world, rank, local):
                            if flush_buf is None else
                            f"flushed: a {2 * l2 / 1e6:.0f} MB buffer is read before every timed step, "
                            f"outside its events (working set {footprint / 1e6:.0f} MB)")),
-        # per step: layout (+ its error fold), notify, [notify_expert: 3,] dispatch, combine;
+        # per step: layout (+ its error fold), notify, [notify_expert: 2,] dispatch, combine;
         # the fused path: prep + fused launch, combine
-        "gpu_launches": (3 if args.fused else (8 if expert else 5)) * args.steps,
+        "gpu_launches": (3 if args.fused else (7 if expert else 5)) * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "traffic": recorded_traffic(traffic_key(args.workload, args.tokens_per_rank, args.layout),

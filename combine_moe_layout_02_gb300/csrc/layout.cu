@@ -28,8 +28,15 @@
 //    shared memory, in CTA order, each CTA writing a share of the source
 //    rank's num_tokens_per_rank / num_tokens_per_expert row. No second pass
 //    over global memory and no cross-cluster synchronisation.
+//  * A source rank held by one CTA (T <= 256 tokens) skips the cluster
+//    exchange: its totals go straight from shared memory.
 //  * A one-block tail kernel folds the clusters' out-of-range flags into the
-//    caller's error word (only when an error word is given).
+//    caller's error word (only when an error word is given). It lets the next
+//    kernel be scheduled at once, then waits for layout_kernel. (The fold can
+//    be done inside layout_kernel, by the last source rank to finish, with a
+//    counter in scratch; measured on GB300, the next kernel, moe_notify's,
+//    then runs up to twice as slowly when its grid waits on layout_kernel's
+//    directly, which costs more than this launch at every size measured.)
 #include "moe_device.cuh"
 
 namespace moe {
@@ -281,6 +288,25 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
     if (tid == 0) tot[P + E] = any_bad;
     MOE_STAMP(3);
 
+    if (cs == 1) {  // the CTA holds the whole source rank: no cluster exchange
+        if (last_n > 0) {
+            write_itr_span(itr + last_g0 * P, tile_bits, last_n, P, W, tid, tb);
+            if (bits) {
+                uint32_t* dst = bits + last_g0 * W;
+                for (int i = tid; i < last_n * W; i += tb) dst[i] = tile_bits[i];
+            }
+        }
+        for (int j = tid; j < P + E; j += tb) {
+            if (j < P)
+                ntpr[s * P + j] = tot[j];
+            else
+                ntpe[s * E + (j - P)] = tot[j];
+        }
+        if (tid == 0 && bad_flags) bad_flags[s] = any_bad != 0;
+        MOE_STAMP(7);
+        MOE_PROF_END();
+        return;
+    }
     // Cluster reduction: CTA r sums columns [r*span, (r+1)*span) over the
     // cluster's CTAs in CTA order. Each (column, peer) pair is read by its
     // own thread, then summed from shared memory.
@@ -325,10 +351,14 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
     MOE_PROF_END();
 }
 
-// Fold the per-source out-of-range flags into the caller's error word.
+// Fold the per-source out-of-range flags into the caller's error word. It
+// lets the next kernel be scheduled before it waits for layout_kernel, so that
+// launch overlaps layout_kernel rather than following it; the next kernel
+// still waits for this grid to complete before it touches global memory.
 __global__ void __launch_bounds__(256)
 layout_err_kernel(int32_t P, const int32_t* __restrict__ bad_flags, int32_t* __restrict__ err) {
-    pdl_wait_then_release();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int bad = 0;
     for (int i = threadIdx.x; i < P; i += blockDim.x) bad |= bad_flags[i];
     bad = __syncthreads_or(bad);

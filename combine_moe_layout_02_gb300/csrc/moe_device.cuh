@@ -152,7 +152,8 @@ __host__ __device__ __forceinline__ void split_range(int64_t n, int64_t b, int64
 //   slots[(kernel * kProfCtas + b) * kProfPhases ...]
 // of the array attached with moe_profile_attach: slot 0 = %globaltimer (ns) at
 // MOE_PROF_BEGIN, slot p = clock64 cycles from MOE_PROF_BEGIN to the end of
-// phase p (0 if not reached). CTAs at or beyond kProfCtas record nothing.
+// phase p (0 if not reached), and the last slot 1 + the SM the CTA ran on
+// (%smid). CTAs at or beyond kProfCtas record nothing.
 // Loop phases that repeat inside a CTA (the int8 consumer's per-token steps)
 // are summed in registers by one thread and written with MOE_PROF_PUT, the
 // start stamp alone then being published with MOE_PROF_END_N(1).
@@ -170,6 +171,11 @@ __device__ __forceinline__ unsigned long long prof_globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+__device__ __forceinline__ unsigned long long prof_smid() {
+    unsigned int v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
+}
 __device__ __forceinline__ unsigned long long* prof_row(int kernel) {
     unsigned long long* p = g_prof_slots;
     if (p == nullptr || blockIdx.x >= static_cast<unsigned>(kProfCtas)) return nullptr;
@@ -182,6 +188,7 @@ __device__ __forceinline__ unsigned long long* prof_row(int kernel) {
     if (threadIdx.x == 0) {                                                           \
         moe_prof_sm_[0] = ::moe::prof_globaltimer();                                  \
         for (int moe_i_ = 1; moe_i_ < kProfPhases; ++moe_i_) moe_prof_sm_[moe_i_] = 0; \
+        moe_prof_sm_[kProfPhases - 1] = ::moe::prof_smid() + 1;                         \
     }
 #define MOE_STAMP(phase)                                                              \
     do {                                                                              \
@@ -191,7 +198,10 @@ __device__ __forceinline__ unsigned long long* prof_row(int kernel) {
 #define MOE_PROF_END_N(n)                                                             \
     do {                                                                              \
         if (moe_prof_row_ && threadIdx.x == 0)                                        \
+        {                                                                             \
             for (int moe_i_ = 0; moe_i_ < (n); ++moe_i_) moe_prof_row_[moe_i_] = moe_prof_sm_[moe_i_]; \
+            moe_prof_row_[kProfPhases - 1] = moe_prof_sm_[kProfPhases - 1];           \
+        }                                                                             \
     } while (0)
 #define MOE_PROF_END() MOE_PROF_END_N(kProfPhases)
 #define MOE_PROF_CLOCK() clock64()

@@ -52,13 +52,13 @@ static_assert(kNotifyCache == 4, "the second pass selects among exactly four cac
 constexpr int kNotifyChanBuf = 4096;     // int32 entries of the channel-start buffer
 
 struct NotifySmem {
-    size_t wcnt, xc, xr, tmp_r, base, total, rprev, ecnt, nrt64, chv, bytes;
+    size_t wcnt, xc, xr, tmp_r, base, total, rprev, ecnt, chv, bytes;
 };
 
 // Shared memory (int32 unless noted): wcnt [warps][P]; xc, xr [cs][P] (the
 // cluster CTAs' totals and rank-prefix partials; this CTA's own row is the
 // one peers read); tmp_r [threads] int4; base [P];
-// total [P]; rprev [P]; ecnt [E/P]; nrt64 int64 [P]; chv [channels starting
+// total [P]; rprev [P]; ecnt [E/P]; chv [channels starting
 // in this CTA's tokens][P] when that fits kNotifyChanBuf.
 __host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs) {
     NotifySmem m;
@@ -76,7 +76,6 @@ __host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs) {
     m.total = take(static_cast<size_t>(P) * 4);
     m.rprev = take(static_cast<size_t>(P) * 4);
     m.ecnt = take(static_cast<size_t>(E / P) * 4);
-    m.nrt64 = take(static_cast<size_t>(P) * 8);
     m.chv = take(kNotifyChanBuf * 4);
     m.bytes = o;
     return m;
@@ -175,7 +174,6 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     int32_t* total = reinterpret_cast<int32_t*>(smem + M.total);
     int32_t* rprev = reinterpret_cast<int32_t*>(smem + M.rprev);
     int32_t* ecnt = reinterpret_cast<int32_t*>(smem + M.ecnt);
-    int64_t* nrt64 = reinterpret_cast<int64_t*>(smem + M.nrt64);
     int32_t* chv = reinterpret_cast<int32_t*>(smem + M.chv);
     int32_t* ctot = xc + r * P;   // this CTA's totals (read by the peers)
     int32_t* rpart = xr + r * P;  // this CTA's rank-prefix partial (read by the peers)
@@ -355,6 +353,33 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     __syncthreads();
     MOE_STAMP(5);
 
+    // --- per-rank outputs (from the prefixes and totals alone) -----------
+    if (r == cs - 1) {
+        // Channels that end at T (the last, and empty trailing ones when T < C)
+        // and channels that start at T (empty ones).
+        const int32_t cl = T < C ? (T > 0 ? T - 1 : 0) : C - 1;
+        const int32_t cb = T < C ? T : C;
+        for (int d = tid; d < P; d += kNotifyThreads) {
+            const int32_t tot = total[d], rp = rprev[d];
+            rpm[s * P + d] = rp + tot;
+            for (int32_t c = cl; c < C; ++c) cpm[(static_cast<int64_t>(s) * P + d) * C + c] = tot;
+            for (int32_t c = cb; c < C; ++c) rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rp + tot;
+            if (s == P - 1) nrt[d] = rp + tot;
+        }
+    }
+    if (s == P - 1 && r == 0 && warp == 0) {
+        // Packed partition bases: the exclusive scan of the receive totals.
+        int64_t run = 0;
+        for (int d0 = 0; d0 < P; d0 += 32) {
+            const int dd = d0 + lane;
+            const int64_t v = dd < P ? static_cast<int64_t>(rprev[dd]) + total[dd] : 0;
+            const int64_t incl = warp_inclusive_scan(v, lane);
+            if (dd < P) part_row_base[dd] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) part_row_base[P] = run;
+    }
+
     // --- 3. heads ------------------------------------------------------------
     // Channels that start inside this CTA's tokens [cta_b, cta_e): their
     // counts go to chv (written out coalesced below) when they fit.
@@ -383,6 +408,7 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
         // Next channel start at or after this lane's token (nb = T: none).
         int32_t nc = sb + tk < se ? next_channel(sb + tk, cq, cr) : C;
         int32_t nb = channel_begin(nc, cq, cr);
+        MOE_STAMP(8);
         // One step: tpw tokens, this lane's token t and flags f.
         auto step = [&](int32_t t, uint32_t f) {
             const bool tv = gvalid && t < se;
@@ -441,8 +467,10 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
             step(t, f);
         }
     }
+    MOE_STAMP(9);
     if (buffered) {
         __syncthreads();
+        MOE_STAMP(10);
         // recv_channel_prefix_matrix[d][s][c] and channel_prefix_matrix[s][d][c-1]
         // for the channels starting here: c runs fastest, so consecutive
         // threads write consecutive entries of a row.
@@ -457,37 +485,6 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     }
 
     MOE_STAMP(6);
-    // --- 4. per-rank outputs ------------------------------------------------
-    if (r == cs - 1) {
-        // Channels that end at T (the last, and empty trailing ones when T < C)
-        // and channels that start at T (empty ones).
-        const int32_t cl = T < C ? (T > 0 ? T - 1 : 0) : C - 1;
-        const int32_t cb = T < C ? T : C;
-        for (int d = tid; d < P; d += kNotifyThreads) {
-            const int32_t tot = total[d], rp = rprev[d];
-            rpm[s * P + d] = rp + tot;
-            for (int32_t c = cl; c < C; ++c) cpm[(static_cast<int64_t>(s) * P + d) * C + c] = tot;
-            for (int32_t c = cb; c < C; ++c) rcpm[(static_cast<int64_t>(d) * P + s) * C + c] = rp + tot;
-            if (s == P - 1) {
-                nrt[d] = rp + tot;
-                nrt64[d] = rp + tot;
-            }
-        }
-        if (s == P - 1) {
-            __syncthreads();
-            if (warp == 0) {
-                int64_t run = 0;
-                for (int d0 = 0; d0 < P; d0 += 32) {
-                    const int dd = d0 + lane;
-                    const int64_t v = dd < P ? nrt64[dd] : 0;
-                    const int64_t incl = warp_inclusive_scan(v, lane);
-                    if (dd < P) part_row_base[dd] = run + incl - v;
-                    run += __shfl_sync(0xffffffffu, incl, 31);
-                }
-                if (lane == 0) part_row_base[P] = run;
-            }
-        }
-    }
     cluster_wait();
     MOE_STAMP(7);
     MOE_PROF_END();

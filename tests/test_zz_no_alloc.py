@@ -92,7 +92,8 @@ def test_static_scratch_layout_matches_moe_layout_and_oracle():
 
 def test_static_scratch_reports_out_of_range_ids():
     """The flags in the shared buffer carry an out-of-range id into err, and the
-    next clean call on the same stream clears it again."""
+    next clean call on the same stream clears it again; a bad id on several
+    source ranks at once, and on the last one alone, is reported as well."""
     import torch
 
     dev = torch.device("cuda", 0)
@@ -101,13 +102,23 @@ def test_static_scratch_reports_out_of_range_ids():
     shape = moe.make_shape(w.P, w.E, w.S, w.K, w.H, w.C, w.expert_alignment, 0)
     bad = w.topk_idx.copy()
     bad[17, 3] = w.E  # one id past the last expert, on source rank 0
-    o_bad, o_ok = _outputs(shape, dev), _outputs(shape, dev)
-    assert _call_static(shape, torch.from_numpy(bad).to(dev), o_bad, stream) == moe.MOE_OK
-    assert _call_static(shape, torch.from_numpy(w.topk_idx).to(dev), o_ok, stream) == moe.MOE_OK
+    many = w.topk_idx.copy()
+    T = w.S // w.P
+    for s_ in (0, 5, w.P - 1):
+        many[s_ * T + 3, 0] = w.E + s_
+    last = w.topk_idx.copy()
+    last[w.S - 1, w.K - 1] = 1 << 30  # the last source rank alone
+    o_bad, o_ok, o_many, o_last, o_ok2 = (_outputs(shape, dev) for _ in range(5))
+    for arr, o in ((bad, o_bad), (w.topk_idx, o_ok), (many, o_many), (last, o_last), (w.topk_idx, o_ok2)):
+        assert _call_static(shape, torch.from_numpy(arr).to(dev), o, stream) == moe.MOE_OK
     torch.cuda.synchronize(dev)
     assert int(o_bad["err"][0].item()) == moe.MOE_ERR_TOPK_OUT_OF_RANGE
     assert int(o_ok["err"][0].item()) == moe.MOE_OK
+    assert int(o_many["err"][0].item()) == moe.MOE_ERR_TOPK_OUT_OF_RANGE
+    assert int(o_last["err"][0].item()) == moe.MOE_ERR_TOPK_OUT_OF_RANGE
+    assert int(o_ok2["err"][0].item()) == moe.MOE_OK
     _check_against_oracle(w, o_ok)
+    _check_against_oracle(w, o_ok2)
 
 
 def test_static_scratch_rejects_shapes_beyond_its_buffer():
