@@ -296,6 +296,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
                 for (int i = tid; i < last_n * W; i += tb) dst[i] = tile_bits[i];
             }
         }
+        MOE_STAMP(4);  // phases 4 and 5 (the cluster exchange) end here
+        MOE_STAMP(5);
         for (int j = tid; j < P + E; j += tb) {
             if (j < P)
                 ntpr[s * P + j] = tot[j];
@@ -303,6 +305,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
                 ntpe[s * E + (j - P)] = tot[j];
         }
         if (tid == 0 && bad_flags) bad_flags[s] = any_bad != 0;
+        MOE_STAMP(6);
         MOE_STAMP(7);
         MOE_PROF_END();
         return;

@@ -118,10 +118,24 @@ __device__ __forceinline__ int32_t channel_begin(int32_t c, int32_t q, int32_t r
     return c * q + min(c, rr);
 }
 
-// The first channel that starts at or after token t.
-__device__ __forceinline__ int32_t next_channel(int32_t t, int32_t q, int32_t rr) {
+// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31, with m = div_magic(d) =
+// ceil(2^32 / d) from the host: the multiply-shift estimate is the quotient
+// or one more (the error term is below n / 2^32 < 1/2), so one correction.
+__device__ __forceinline__ int32_t div_m(int32_t n, int32_t d, uint64_t m) {
+    uint32_t q = static_cast<uint32_t>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * m) >> 32);
+    if (q * static_cast<uint32_t>(d) > static_cast<uint32_t>(n)) --q;
+    return static_cast<int32_t>(q);
+}
+inline uint64_t div_magic(int32_t d) {
+    const uint64_t dd = static_cast<uint64_t>(d < 1 ? 1 : d);
+    return ((uint64_t{1} << 32) + dd - 1) / dd;
+}
+
+// The first channel that starts at or after token t < T; m1 = div_magic(q + 1),
+// m0 = div_magic(q) (q >= 1 whenever t >= rr * (q + 1)).
+__device__ __forceinline__ int32_t next_channel(int32_t t, int32_t q, int32_t rr, uint64_t m1, uint64_t m0) {
     const int32_t bnd = rr * (q + 1);  // tokens in the rr longer channels
-    int32_t c = t < bnd ? t / (q + 1) : rr + (t - bnd) / q;
+    int32_t c = t < bnd ? div_m(t, q + 1, m1) : rr + div_m(t - bnd, q, m0);
     if (channel_begin(c, q, rr) < t) ++c;
     return c;
 }
@@ -139,6 +153,12 @@ struct NotifyParams {
     const uint8_t* itr;
     int32_t *rpm, *cpm, *rcpm, *nrt, *nrtpe, *reo, *send_head;
     int64_t* part_row_base;
+    uint64_t mq1, mq0;  // div_magic(cq + 1), div_magic(cq)
+    // notify_small_kernel only: log2 of the lanes per token, rows of the two
+    // partial-sum tables, division constants, shared-memory offsets (bytes)
+    int32_t lg, sR, sRq;
+    uint64_t mP, mE, mA;
+    int32_t off_wcnt, off_rpart, off_epart, off_rprev, off_total, off_ecnt, off_chv;
 };
 
 // Grid: P clusters of cs CTAs of kNotifyThreads threads; cluster s handles
@@ -386,8 +406,8 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     const int32_t cta_b = r * kNotifyWarps * a.wq + min(r * kNotifyWarps, a.wr);
     const int32_t cta_e = min(T, cta_b + kNotifyWarps * a.wq + max(0, min(kNotifyWarps, a.wr - r * kNotifyWarps)));
     const int32_t nonempty = min(T, C);  // channels that start before T
-    const int32_t c_lo = cta_b < T ? next_channel(cta_b, cq, cr) : nonempty;
-    const int32_t c_hi = cta_e < T ? next_channel(cta_e, cq, cr) : nonempty;
+    const int32_t c_lo = cta_b < T ? next_channel(cta_b, cq, cr, a.mq1, a.mq0) : nonempty;
+    const int32_t c_hi = cta_e < T ? next_channel(cta_e, cq, cr, a.mq1, a.mq0) : nonempty;
     const bool buffered = static_cast<int64_t>(c_hi - c_lo) * P <= kNotifyChanBuf;
     for (int rb = 0; rb * 32 < G; ++rb) {
         const int gn = min(32, G - rb * 32);
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
             rp[j] = ok ? rprev[d + j] : 0;
         }
         // Next channel start at or after this lane's token (nb = T: none).
-        int32_t nc = sb + tk < se ? next_channel(sb + tk, cq, cr) : C;
+        int32_t nc = sb + tk < se ? next_channel(sb + tk, cq, cr, a.mq1, a.mq0) : C;
         int32_t nb = channel_begin(nc, cq, cr);
         MOE_STAMP(8);
         // One step: tpw tokens, this lane's token t and flags f.
@@ -490,13 +510,307 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     MOE_PROF_END();
 }
 
+// ---------------------------------------------------------------------------
+// Small source ranks: one CTA of kSmallThreads threads holds all T tokens of
+// rank s (each warp's tokens in at most kNotifyCache steps), so no cluster
+// exchange is needed. Every reduction is a warp of lanes with shuffles, run
+// side by side after one block barrier:
+//   - per rank d, the exclusive offsets of the warps' counts (lane = warp);
+//   - per rank d, the column sum of num_tokens_per_rank over the source ranks
+//     before s (partial sums of kSmallThreads / P rows each, then the lanes);
+//   - per local expert l, the sum of num_tokens_per_expert[.][s * E/P + l] over
+//     the source ranks, rounded up to expert_alignment.
+// The heads pass and the channel matrices follow the cluster kernel above.
+// 512 threads measured fastest on GB300 (p32_e256_t128: front 10.8 us at
+// 512, 12.0 at 1024, 12.9 at 256; tiny_p4_e16: 7.8, 8.9, 7.5): more warps
+// repeat the per-warp set-up, fewer lengthen each warp's chain.
+#ifndef MOE_NOTIFY_SMALL_THREADS
+#define MOE_NOTIFY_SMALL_THREADS 512
+#endif
+constexpr int kSmallThreads = MOE_NOTIFY_SMALL_THREADS;
+constexpr int kSmallWarps = kSmallThreads / 32;
+static_assert(kSmallWarps <= 32 && kSmallThreads % 32 == 0, "the warp-offset scan puts one warp per lane");
+
+struct SmallSmem {
+    size_t wcnt, rpart, epart, rprev, total, ecnt, chv, bytes;
+};
+
+// wcnt [warps][P]; rpart [kSmallThreads / P][P]; epart [kSmallThreads / epr][epr];
+// rprev, total [P]; ecnt [epr]; chv [channels][P] when that fits kNotifyChanBuf.
+__host__ __device__ inline SmallSmem small_smem(int P, int E) {
+    SmallSmem m;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += (bytes + 15) / 16 * 16;
+        return at;
+    };
+    const int epr = E / P;
+    m.wcnt = take(static_cast<size_t>(kSmallWarps) * P * 4);
+    m.rpart = take(static_cast<size_t>(kSmallThreads / P) * P * 4);
+    m.epart = take(static_cast<size_t>(kSmallThreads / epr) * epr * 4);
+    m.rprev = take(static_cast<size_t>(P) * 4);
+    m.total = take(static_cast<size_t>(P) * 4);
+    m.ecnt = take(static_cast<size_t>(epr) * 4);
+    m.chv = take(kNotifyChanBuf * 4);
+    m.bytes = o;
+    return m;
+}
+
+// Grid: P CTAs; CTA s handles source rank s. The warps' token segments are
+// the balanced split of T over 32 warps (wq, wr).
+template <bool A4>
+__global__ void __launch_bounds__(kSmallThreads, 1) notify_small_kernel(const NotifyParams a) {
+    pdl_wait_then_release();
+    MOE_PROF_BEGIN(kProfNotify);
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int32_t P = a.P, E = a.E, C = a.C, A = a.A, T = a.T, epr = a.epr;
+    const int32_t* __restrict__ ntpr = a.ntpr;
+    const int32_t* __restrict__ ntpe = a.ntpe;
+    int32_t* __restrict__ rpm = a.rpm;
+    int32_t* __restrict__ cpm = a.cpm;
+    int32_t* __restrict__ rcpm = a.rcpm;
+    int32_t* __restrict__ send_head = a.send_head;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t s = static_cast<int32_t>(blockIdx.x);
+    int32_t* wcnt = reinterpret_cast<int32_t*>(smem + a.off_wcnt);
+    int32_t* rpart = reinterpret_cast<int32_t*>(smem + a.off_rpart);
+    int32_t* epart = reinterpret_cast<int32_t*>(smem + a.off_epart);
+    int32_t* rprev = reinterpret_cast<int32_t*>(smem + a.off_rprev);
+    int32_t* total = reinterpret_cast<int32_t*>(smem + a.off_total);
+    int32_t* ecnt = reinterpret_cast<int32_t*>(smem + a.off_ecnt);
+    int32_t* chv = reinterpret_cast<int32_t*>(smem + a.off_chv);
+
+    const int G = (P + 3) >> 2;  // rank groups of 4 (<= 32 here)
+    const int lg = a.lg, L = 1 << lg;  // lanes per token: the power of two >= G
+    const int tpw = 32 >> lg;
+    const int g = lane & (L - 1), tk = lane >> lg;
+    const int d = 4 * g;
+    const bool gvalid = g < G;
+    const int32_t sb = warp * a.wq + min(warp, a.wr);
+    const int32_t se = sb + a.wq + (warp < a.wr ? 1 : 0);
+    const uint8_t* src_rows = a.itr + static_cast<int64_t>(s) * T * P;
+
+    // --- loads -------------------------------------------------------------
+    // rank-prefix partials: column dc over rows rr, rr + R, ... < s
+    const int R = a.sR;
+    const int rr = div_m(tid, P, a.mP), dc = tid - rr * P;
+    int32_t racc = 0;
+    if (rr < R)
+        for (int32_t q = rr; q < s; q += R) racc += __ldg(ntpr + static_cast<int64_t>(q) * P + dc);
+    // expert partials: local expert lc over source ranks qr, qr + Rq, ... < P
+    const int Rq = a.sRq;
+    const int qr = div_m(tid, epr, a.mE), lc = tid - qr * epr;
+    int32_t eacc = 0;
+    if (qr < Rq)
+        for (int32_t q = qr; q < P; q += Rq) eacc += __ldg(ntpe + static_cast<int64_t>(q) * E + s * epr + lc);
+    // this lane's flags, kept for the heads pass
+    uint32_t fc[kNotifyCache];
+#pragma unroll
+    for (int i = 0; i < kNotifyCache; ++i) {
+        const int32_t t = sb + tk + i * tpw;
+        fc[i] = (gvalid && t < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P) : 0u;
+    }
+    // --- count -------------------------------------------------------------
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll
+    for (int i = 0; i < kNotifyCache; ++i) {
+        c0 += byte_of(fc[i], 0);
+        c1 += byte_of(fc[i], 1);
+        c2 += byte_of(fc[i], 2);
+        c3 += byte_of(fc[i], 3);
+    }
+    for (int o = L; o < 32; o <<= 1) {
+        c0 += __shfl_xor_sync(0xffffffffu, c0, o);
+        c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+        c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+        c3 += __shfl_xor_sync(0xffffffffu, c3, o);
+    }
+    if (tk == 0 && gvalid) {
+        int32_t* wc = wcnt + warp * P + d;
+        wc[0] = c0;
+        if (d + 1 < P) wc[1] = c1;
+        if (d + 2 < P) wc[2] = c2;
+        if (d + 3 < P) wc[3] = c3;
+    }
+    if (rr < R) rpart[rr * P + dc] = racc;
+    if (qr < Rq) epart[qr * epr + lc] = eacc;
+    MOE_STAMP(1);
+    __syncthreads();
+    MOE_STAMP(2);
+
+    // --- reductions, one warp per task --------------------------------------
+    const int rows_e = min(Rq, P);
+    for (int task = warp; task < 2 * P + epr; task += kSmallWarps) {
+        if (task < P) {  // warp offsets of rank task (lane = warp index)
+            const int32_t v = lane < kSmallWarps ? wcnt[lane * P + task] : 0;
+            const int32_t incl = warp_inclusive_scan(v, lane);
+            if (lane < kSmallWarps) wcnt[lane * P + task] = incl - v;
+            if (lane == 31) total[task] = incl;
+        } else if (task < 2 * P) {  // rank prefix of column task - P
+            const int col = task - P;
+            int32_t sum = 0;
+            for (int r = lane; r < R; r += 32) sum += rpart[r * P + col];
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) rprev[col] = sum;
+        } else {  // receive count of local expert task - 2P
+            const int l = task - 2 * P;
+            int32_t sum = 0;
+            for (int r = lane; r < rows_e; r += 32) sum += epart[r * epr + l];
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) ecnt[l] = div_m(sum + A - 1, A, a.mA) * A;  // fits int32 (shape limits)
+        }
+    }
+    __syncthreads();
+    MOE_STAMP(3);
+
+    // --- per-rank outputs (from the prefixes and totals alone) -------------
+    {
+        const int32_t cl = T < C ? (T > 0 ? T - 1 : 0) : C - 1;
+        const int32_t cb = T < C ? T : C;
+        for (int dd = tid; dd < P; dd += kSmallThreads) {
+            const int32_t tot = total[dd], rp = rprev[dd];
+            rpm[s * P + dd] = rp + tot;
+            for (int32_t c = cl; c < C; ++c) cpm[(static_cast<int64_t>(s) * P + dd) * C + c] = tot;
+            for (int32_t c = cb; c < C; ++c) rcpm[(static_cast<int64_t>(dd) * P + s) * C + c] = rp + tot;
+            if (s == P - 1) a.nrt[dd] = rp + tot;
+        }
+    }
+    if (warp == kSmallWarps - 1) {  // rank s's receive counts per local expert, scanned
+        int32_t carry = 0;
+        for (int l0 = 0; l0 < epr; l0 += 32) {
+            const int l = l0 + lane;
+            const int32_t v = l < epr ? ecnt[l] : 0;
+            const int32_t incl = warp_inclusive_scan(v, lane);
+            if (l < epr) {
+                a.nrtpe[s * epr + l] = v;
+                a.reo[s * epr + l] = carry + incl - v;
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (s == P - 1 && warp == kSmallWarps - 2) {  // packed partition bases
+        int64_t run = 0;
+        for (int d0 = 0; d0 < P; d0 += 32) {
+            const int dd = d0 + lane;
+            const int64_t v = dd < P ? static_cast<int64_t>(rprev[dd]) + total[dd] : 0;
+            const int64_t incl = warp_inclusive_scan(v, lane);
+            if (dd < P) a.part_row_base[dd] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) a.part_row_base[P] = run;
+    }
+
+    // --- heads ---------------------------------------------------------------
+    const int32_t cq = a.cq, cr = a.cr;
+    const int32_t nonempty = min(T, C);  // channels that start before T
+    const bool buffered = static_cast<int64_t>(nonempty) * P <= kNotifyChanBuf;
+    {
+        const int last = (tpw - 1) * L + g;  // lane of this group's last token in a step
+        int run[4], rp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool ok = gvalid && d + j < P;
+            run[j] = ok ? wcnt[warp * P + d + j] : 0;
+            rp[j] = ok ? rprev[d + j] : 0;
+        }
+        int32_t nc = sb + tk < se ? next_channel(sb + tk, cq, cr, a.mq1, a.mq0) : C;
+        int32_t nb = channel_begin(nc, cq, cr);
+#pragma unroll 1
+        for (int32_t i = 0, t0 = sb; t0 < se; ++i, t0 += tpw) {
+            const int32_t t = t0 + tk;
+            const uint32_t f = i == 0 ? fc[0] : (i == 1 ? fc[1] : (i == 2 ? fc[2] : fc[3]));
+            const bool tv = gvalid && t < se;
+            uint32_t incl = f;
+            for (int o = L; o < 32; o <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            const uint32_t excl = incl - f;
+            const uint32_t step_total = L == 32 ? f : __shfl_sync(0xffffffffu, incl, last);
+            if (tv) {
+                int loc[4], v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    loc[j] = run[j] + byte_of(excl, j);
+                    v[j] = byte_of(f, j) ? rp[j] + loc[j] : -1;
+                }
+                int32_t* out = send_head + (static_cast<int64_t>(s) * T + t) * P + d;
+                if (A4) {
+                    *reinterpret_cast<int4*>(out) = make_int4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (d + j < P) out[j] = v[j];
+                }
+                while (nb < t) nb = channel_begin(++nc, cq, cr);
+                if (nb == t) {  // t starts channel nc
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (d + j < P) {
+                            if (buffered) {
+                                chv[nc * P + d + j] = loc[j];
+                            } else {
+                                rcpm[(static_cast<int64_t>(d + j) * P + s) * C + nc] = rp[j] + loc[j];
+                                if (nc > 0) cpm[(static_cast<int64_t>(s) * P + d + j) * C + nc - 1] = loc[j];
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) run[j] += byte_of(step_total, j);
+        }
+    }
+    MOE_STAMP(4);
+    if (buffered) {
+        __syncthreads();
+        // recv_channel_prefix_matrix[d][s][c] and channel_prefix_matrix[s][d][c-1]
+        // for every channel that starts before T, c fastest.
+        for (int dd = warp; dd < P; dd += kSmallWarps) {
+            int32_t* rrow = rcpm + (static_cast<int64_t>(dd) * P + s) * C;
+            int32_t* crow = cpm + (static_cast<int64_t>(s) * P + dd) * C - 1;
+            const int32_t rp = rprev[dd];
+            for (int c = lane; c < nonempty; c += 32) {
+                const int32_t v = chv[c * P + dd];
+                rrow[c] = rp + v;
+                if (c > 0) crow[c] = v;
+            }
+        }
+    }
+    MOE_STAMP(5);
+    MOE_STAMP(6);  // stamps 6 and 7 end the kernel, as in the cluster kernel
+    MOE_STAMP(7);
+    MOE_PROF_END_N(8);
+}
+
 struct NotifyPlan {
+    bool small;  // one CTA per source rank (notify_small_kernel)
     int cluster;
     size_t smem;
 };
 
+// One CTA of kSmallThreads covers a source rank when each of its 32 warps
+// needs at most kNotifyCache steps (the flags stay in registers) and the rank
+// groups fit one warp (P <= 128).
+bool notify_small(const moe_shape& s) {
+    const int64_t T = s.S / s.P;
+    const int G = (s.P + 3) / 4;
+    if (G > 32 || s.E / s.P > kSmallThreads) return false;
+    int L = 1;
+    while (L < G) L <<= 1;
+    return T <= static_cast<int64_t>(kSmallWarps) * (32 / L) * kNotifyCache;
+}
+
 NotifyPlan notify_plan(const moe_shape& s) {
     const int64_t T = s.S / s.P;
+    if (notify_small(s)) {
+        NotifyPlan p;
+        p.small = true;
+        p.cluster = 1;
+        p.smem = small_smem(s.P, s.E).bytes;
+        return p;
+    }
     // Tokens a warp covers per step in the first block of rank groups.
     const int G = (s.P + 3) / 4;
     int L = 1;
@@ -511,6 +825,7 @@ NotifyPlan notify_plan(const moe_shape& s) {
     // the peers' totals and partials (2 x cs x P int32) stay within 64 KB
     while (c > 1 && static_cast<int64_t>(c) * s.P * 8 > 64 * 1024) c >>= 1;
     NotifyPlan p;
+    p.small = false;
     p.cluster = c;
     p.smem = notify_smem(s.P, s.E, c).bytes;
     return p;
@@ -533,14 +848,6 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
     const int64_t T = s.S / s.P;
     const NotifyPlan p = notify_plan(s);
     const bool a4 = (s.P & 3) == 0;
-    const void* fn = a4 ? reinterpret_cast<const void*>(notify_kernel<true>)
-                        : reinterpret_cast<const void*>(notify_kernel<false>);
-    cudaError_t e = prepare_kernel(fn, p.smem, kNotifyThreads, nullptr);
-    if (e != cudaSuccess) return e;
-    const int cs = cluster_size_for(fn, p.cluster, kNotifyThreads, p.smem);
-    if (cs < 1) return cudaErrorInvalidConfiguration;
-    auto kern = a4 ? notify_kernel<true> : notify_kernel<false>;
-    const size_t smem = notify_smem(s.P, s.E, cs).bytes;  // for the cluster size granted
     NotifyParams a{};
     a.P = s.P;
     a.E = s.E;
@@ -548,15 +855,8 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
     a.A = s.expert_alignment;
     a.epr = s.E / s.P;
     a.T = static_cast<int32_t>(T);
-    a.cs = cs;
-    a.lcs = 0;
-    while ((1 << a.lcs) < cs) ++a.lcs;
-    a.wq = static_cast<int32_t>(T / (cs * kNotifyWarps));
-    a.wr = static_cast<int32_t>(T % (cs * kNotifyWarps));
     a.cq = static_cast<int32_t>(T / s.num_channels);
     a.cr = static_cast<int32_t>(T % s.num_channels);
-    a.eq = a.epr / cs;
-    a.er = a.epr % cs;
     a.ntpr = ntpr;
     a.ntpe = ntpe;
     a.itr = itr;
@@ -568,6 +868,50 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
     a.reo = reo;
     a.send_head = send_head;
     a.part_row_base = part_row_base;
+    a.mq1 = div_magic(a.cq + 1);
+    a.mq0 = div_magic(a.cq);
+    if (p.small) {
+        const void* sfn = a4 ? reinterpret_cast<const void*>(notify_small_kernel<true>)
+                             : reinterpret_cast<const void*>(notify_small_kernel<false>);
+        cudaError_t e = prepare_kernel(sfn, p.smem, kSmallThreads, nullptr);
+        if (e != cudaSuccess) return e;
+        a.cs = 1;
+        a.wq = static_cast<int32_t>(T / kSmallWarps);
+        a.wr = static_cast<int32_t>(T % kSmallWarps);
+        const int G = (s.P + 3) / 4;
+        a.lg = 0;
+        while ((1 << a.lg) < G) ++a.lg;
+        a.sR = kSmallThreads / s.P;
+        a.sRq = kSmallThreads / a.epr;
+        a.mP = div_magic(s.P);
+        a.mE = div_magic(a.epr);
+        a.mA = div_magic(s.expert_alignment);
+        const SmallSmem M = small_smem(s.P, s.E);
+        a.off_wcnt = static_cast<int32_t>(M.wcnt);
+        a.off_rpart = static_cast<int32_t>(M.rpart);
+        a.off_epart = static_cast<int32_t>(M.epart);
+        a.off_rprev = static_cast<int32_t>(M.rprev);
+        a.off_total = static_cast<int32_t>(M.total);
+        a.off_ecnt = static_cast<int32_t>(M.ecnt);
+        a.off_chv = static_cast<int32_t>(M.chv);
+        return launch_pdl(a4 ? notify_small_kernel<true> : notify_small_kernel<false>, static_cast<unsigned>(s.P),
+                          kSmallThreads, p.smem, stream, a);
+    }
+    const void* fn = a4 ? reinterpret_cast<const void*>(notify_kernel<true>)
+                        : reinterpret_cast<const void*>(notify_kernel<false>);
+    cudaError_t e = prepare_kernel(fn, p.smem, kNotifyThreads, nullptr);
+    if (e != cudaSuccess) return e;
+    const int cs = cluster_size_for(fn, p.cluster, kNotifyThreads, p.smem);
+    if (cs < 1) return cudaErrorInvalidConfiguration;
+    auto kern = a4 ? notify_kernel<true> : notify_kernel<false>;
+    const size_t smem = notify_smem(s.P, s.E, cs).bytes;  // for the cluster size granted
+    a.cs = cs;
+    a.lcs = 0;
+    while ((1 << a.lcs) < cs) ++a.lcs;
+    a.wq = static_cast<int32_t>(T / (cs * kNotifyWarps));
+    a.wr = static_cast<int32_t>(T % (cs * kNotifyWarps));
+    a.eq = a.epr / cs;
+    a.er = a.epr % cs;
     return launch_pdl_cluster(kern, static_cast<unsigned>(s.P) * cs, kNotifyThreads, smem, cs, stream, a);
 }
 
