@@ -473,18 +473,23 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
 #pragma unroll
             for (int j = 0; j < 4; ++j) run[j] += byte_of(step_total, j);
         };
-        // One copy of the step code: flags from the registers of the count
-        // pass (selected without indexing) or read again.
+        // One copy of the step code. The flags come from the registers of the
+        // count pass (selected without indexing) or, when the segment is
+        // longer, are read again kNotifyCache steps at a time, so that the
+        // loads of four steps are in flight together rather than one L2 round
+        // trip per step.
 #pragma unroll 1
         for (int32_t i = 0, t0 = sb; t0 < se; ++i, t0 += tpw) {
-            const int32_t t = t0 + tk;
-            uint32_t f;
-            if (cached) {
-                f = i == 0 ? fc[0] : (i == 1 ? fc[1] : (i == 2 ? fc[2] : fc[3]));
-            } else {
-                f = (gvalid && t < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P) : 0u;
+            const int k = i & (kNotifyCache - 1);
+            if (!cached && k == 0) {
+#pragma unroll
+                for (int j = 0; j < kNotifyCache; ++j) {
+                    const int32_t tj = t0 + j * tpw + tk;
+                    fc[j] = (gvalid && tj < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(tj) * P, d, P) : 0u;
+                }
             }
-            step(t, f);
+            const uint32_t f = k == 0 ? fc[0] : (k == 1 ? fc[1] : (k == 2 ? fc[2] : fc[3]));
+            step(t0 + tk, f);
         }
     }
     MOE_STAMP(9);
