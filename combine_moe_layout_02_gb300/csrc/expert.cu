@@ -18,8 +18,12 @@
 //     (its row of ecount, 16-byte loads) to recv_expert_offset -- the chunk's
 //     first row of every expert; per-warp histograms of the chunk become
 //     exclusive warp offsets; then each warp ranks its slots 32 at a time in
-//     (token, k) order among the step's slots of the same expert
-//     (__match_any_sync). CTA 0 also scans the rank totals into
+//     (token, k) order among the step's slots of the same expert: each lane
+//     sets its bit in the warp's shared-memory mask of its expert, reads the
+//     mask back (the lanes of its group) and takes the popcount of the lower
+//     lanes; the group's last lane advances the expert's offset and clears the
+//     mask. (__match_any_sync gives the same groups; measured on GB300 it cost
+//     about 1000 cycles a step.) CTA 0 also scans the rank totals into
 //     expert_part_base.
 // Integer counts: the result does not depend on the order of the atomics.
 #include "moe_device.cuh"
@@ -42,19 +46,21 @@ ExpertPlan expert_plan(const moe_shape& s) {
     // One token per thread and about 64 chunks (measured best at S = 4096,
     // 32768 and 65536: fewer chunks leave SMs idle, more lengthen each CTA's
     // prefix over the earlier chunks): a power of two from 256 to kChunk, no
-    // more than S needs, and few enough warps that their histograms
-    // ([warps][E]) stay within 128 KB.
+    // more than S needs, and few enough warps that their histograms and group
+    // masks (2 x [warps][E]) stay within 128 KB.
     int64_t t = 256;
     while (t < kChunk && t * 64 < s.S) t <<= 1;
     if (t > s.S) t = round_up(s.S > 0 ? s.S : 1, 32);
-    const int64_t by_smem = (128 * 1024 / (static_cast<int64_t>(s.E) * 4)) / 1 * 32;
+    const int64_t by_smem = (128 * 1024 / (static_cast<int64_t>(s.E) * 8)) * 32;
     if (t > by_smem) t = by_smem < 32 ? 32 : by_smem / 32 * 32;
     p.threads = static_cast<int>(t);
     p.chunks = ceil_div(s.S, t);
     p.chunks_pad = round_up(p.chunks, 4);
     p.smem_count = static_cast<size_t>(s.E) * 4;
-    // per-warp histograms [warps][E], the chunk's bases [E] and slot ids [threads][K]
-    p.smem_rows = (static_cast<size_t>(p.threads / 32) + 1) * s.E * 4 + static_cast<size_t>(p.threads) * s.K * 4;
+    // per-warp histograms [warps][E], the chunk's bases [E], slot ids
+    // [threads][K] and per-warp group masks [warps][E]
+    p.smem_rows = (static_cast<size_t>(p.threads / 32) + 1) * s.E * 4 + static_cast<size_t>(p.threads) * s.K * 4 +
+                  static_cast<size_t>(p.threads / 32) * s.E * 4;
     p.scratch_bytes = round_up(static_cast<int64_t>(s.E) * p.chunks_pad * 4, 256);
     return p;
 }
@@ -89,6 +95,7 @@ __global__ void __launch_bounds__(kChunk)
 expert_count_kernel(int32_t E, int32_t K, int64_t S, int64_t chunks_pad, const int32_t* __restrict__ topk_idx,
                     int32_t* __restrict__ ecount) {
     pdl_wait_then_release();
+    MOE_PROF_BEGIN(kProfExpertCount);
     extern __shared__ __align__(16) int32_t hist[];  // [E]
     const int tid = threadIdx.x;
     const int64_t chunk = blockIdx.x;
@@ -100,8 +107,11 @@ expert_count_kernel(int32_t E, int32_t K, int64_t S, int64_t chunks_pad, const i
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k)
         if (k < K && ids[k] >= 0) atomicAdd(hist + ids[k], 1);
+    MOE_STAMP(1);
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) ecount[static_cast<int64_t>(e) * chunks_pad + chunk] = hist[e];
+    MOE_STAMP(2);
+    MOE_PROF_END_N(3);
 }
 
 __global__ void __launch_bounds__(kChunk)
@@ -110,12 +120,14 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
                    const int32_t* __restrict__ reo, const int32_t* __restrict__ nrtpe, int32_t* __restrict__ slot_row,
                    int64_t* __restrict__ expert_part_base) {
     pdl_wait_then_release();
+    MOE_PROF_BEGIN(kProfNotifyExpert);
     extern __shared__ __align__(16) int32_t sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     int32_t* whist = sm;                       // [nwarps][E]: counts, then each warp's first rows
     int32_t* cbase = sm + nwarps * E;          // [E]: the chunk's first row of each expert
     int32_t* sids = cbase + E;                 // [threads][K]: the chunk's slot ids in (token, k) order
+    uint32_t* gmask = reinterpret_cast<uint32_t*>(sids + blockDim.x * K);  // [nwarps][E]: lanes per expert
     const int64_t chunk = blockIdx.x;
     const int64_t g0 = chunk * blockDim.x;
     const bool work = chunk < chunks;
@@ -141,7 +153,10 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
             if (lane == 0) expert_part_base[P] = run;
         }
     }
-    if (!work) return;
+    if (!work) {
+        MOE_PROF_END_N(1);
+        return;
+    }
 
     const int64_t g = g0 + tid;
     int32_t ids[MOE_MAX_TOPK];
@@ -152,7 +167,7 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
         int32_t acc = __ldg(reo + e);
         const int32_t* row = ecount + static_cast<int64_t>(e) * chunks_pad;
         int64_t c = 0;
-#pragma unroll 4
+#pragma unroll 16
         for (; c + 4 <= chunk; c += 4) {
             const int4 v = __ldg(reinterpret_cast<const int4*>(row + c));
             acc += v.x + v.y + v.z + v.w;
@@ -160,7 +175,11 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
         for (; c < chunk; ++c) acc += __ldg(row + c);
         cbase[e] = acc;
     }
-    for (int i = tid; i < nwarps * E; i += blockDim.x) whist[i] = 0;
+    MOE_STAMP(1);
+    for (int i = tid; i < nwarps * E; i += blockDim.x) {
+        whist[i] = 0;
+        gmask[i] = 0u;
+    }
     int32_t* srow = sids + tid * K;
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k)
@@ -171,6 +190,7 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
     for (int k = 0; k < MOE_MAX_TOPK; ++k)
         if (k < K && ids[k] >= 0) atomicAdd(my + ids[k], 1);
     __syncthreads();
+    MOE_STAMP(2);
     // Exclusive warp offsets per expert, from the chunk base.
     for (int e = tid; e < E; e += blockDim.x) {
         int32_t run = cbase[e];
@@ -181,23 +201,36 @@ expert_rows_kernel(int32_t P, int32_t E, int32_t K, int64_t S, int64_t chunks, i
         }
     }
     __syncthreads();
+    MOE_STAMP(3);
     // Rank each slot among the earlier slots of its expert, 32 slots a step.
     const int64_t wg0 = g0 + warp * 32;  // the warp's first token
     const int ntok = static_cast<int>(min(static_cast<int64_t>(32), S - wg0));
-    if (ntok <= 0) return;
+    if (ntok <= 0) {
+        MOE_STAMP(4);
+        MOE_PROF_END_N(5);
+        return;
+    }
     const int nslots = ntok * K;
     const int32_t* wids = sids + warp * 32 * K;
     int32_t* out = slot_row + wg0 * K;
     const uint32_t below = lanemask_lt();
+    uint32_t* wm = gmask + warp * E;
     for (int f0 = 0; f0 < nslots; f0 += 32) {
         const int f = f0 + lane;
         const int32_t e = f < nslots ? wids[f] : -1;
-        const uint32_t grp = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) atomicOr(wm + e, 1u << lane);
+        __syncwarp();
+        const uint32_t grp = e >= 0 ? wm[e] : 0u;  // the lanes of this step with expert e
         if (f < nslots) out[f] = e >= 0 ? my[e] + __popc(grp & below) : -1;
         __syncwarp();
-        if (e >= 0 && lane == 31 - __clz(grp)) my[e] += __popc(grp);
+        if (e >= 0 && lane == 31 - __clz(grp)) {
+            my[e] += __popc(grp);
+            wm[e] = 0u;
+        }
         __syncwarp();
     }
+    MOE_STAMP(4);
+    MOE_PROF_END_N(5);
 }
 
 }  // namespace

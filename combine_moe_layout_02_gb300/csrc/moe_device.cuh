@@ -162,7 +162,7 @@ constexpr int kProfKernels = MOE_PROF_KERNELS;
 constexpr int kProfCtas = MOE_PROF_CTAS;
 constexpr int kProfPhases = MOE_PROF_PHASES;
 enum ProfKernel { kProfLayout = 0, kProfNotify = 1, kProfDispatch = 2, kProfDispatchInt8 = 3, kProfCombine = 4,
-                  kProfFused = 5, kProfNotifyExpert = 6 };
+                  kProfFused = 5, kProfNotifyExpert = 6, kProfExpertCount = 7 };
 // One copy per translation unit, set by that unit's prof_attach_* function.
 static __device__ unsigned long long* g_prof_slots;
 
