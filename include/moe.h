@@ -472,9 +472,10 @@ moe_status moe_test_fused_barrier(uint32_t spin_limit, int32_t skip_cta);
  *           or, for the int8 consumer's per-token steps, that step's cycles
  *           summed over the CTA's first consumer warp's tokens (added to:
  *           clear the array before a run).
- * Kernel ids: 0 layout, 1 notify, 2 dispatch bf16, 3 dispatch int8,
- * 4 combine, 5 fused, 6 notify_expert. CTAs at or beyond MOE_PROF_CTAS record
- * nothing. Synchronous (a copy to each kernel unit's device pointer); call it
+ *   slot MOE_PROF_PHASES - 1: 1 + the SM the CTA ran on (%smid).
+ * Kernel ids: 0 layout, 1 notify (either kernel), 2 dispatch bf16, 3 dispatch
+ * int8, 4 combine, 5 fused, 6 notify_expert's rows kernel, 7 its count
+ * kernel. CTAs at or beyond MOE_PROF_CTAS record nothing. Synchronous (a copy to each kernel unit's device pointer); call it
  * with no work of this library in flight. Outputs are unchanged.
  */
 #define MOE_PROF_KERNELS 8
