@@ -373,6 +373,54 @@ def workload_config(name, T=None):
 # --------------------------------------------------------------------------
 # Our arm.
 
+def host_link_ceiling(dev, x_host, idx_host, wts_host, out_host, out, reps: int = 5):
+    """The host link's sustained rate for the step's copies alone: the inputs
+    host->device (x, topk_idx, topk_weights from pinned memory), the output
+    device->host, and both at once on two streams. Each timing repeats the
+    copies until at least 256 MB have moved in each direction (a small step's
+    copies alone are latency-bound); best of `reps`, wall clock with a device
+    synchronisation on both sides; GB/s."""
+    import torch
+
+    dx, di, dw = torch.empty_like(x_host, device=dev), torch.empty_like(idx_host, device=dev), \
+        torch.empty_like(wts_host, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    b_in = x_host.numel() * 2 + idx_host.numel() * 4 + wts_host.numel() * 4
+    b_out = out_host.numel() * 2
+    n_in = max(1, -(-(256 << 20) // b_in))
+    n_out = max(1, -(-(256 << 20) // b_out))
+
+    def copy_in():
+        with torch.cuda.stream(s_in):
+            for _ in range(n_in):
+                dx.copy_(x_host, non_blocking=True)
+                di.copy_(idx_host, non_blocking=True)
+                dw.copy_(wts_host, non_blocking=True)
+
+    def copy_out():
+        with torch.cuda.stream(s_out):
+            for _ in range(n_out):
+                out_host.copy_(out, non_blocking=True)
+
+    def best(fn):
+        t = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            t = min(t, time.perf_counter() - t0)
+        return t
+
+    t_in, t_out = best(copy_in), best(copy_out)
+    t_both = best(lambda: (copy_in(), copy_out()))
+    del dx, di, dw
+    return {"h2d_gbs": n_in * b_in / t_in / 1e9, "d2h_gbs": n_out * b_out / t_out / 1e9,
+            "concurrent_gbs": (n_in * b_in + n_out * b_out) / t_both / 1e9,
+            "method": "the step's pinned copies repeated to >= 256 MB per direction, alone and on two "
+                      "streams at once, best of 5, wall clock"}
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -592,6 +640,9 @@ def run_ours(args, world, rank, local):
     e_max, e_units = aggregate(e_elapsed, float(w.S * e2e_steps), world)
     if int(buf.err[0].item()) != 0:
         raise RuntimeError(f"device error {moe.status_string(int(buf.err[0].item()))}")
+    link = host_link_ceiling(dev, x_host, idx_host, wts_host, out_host, out)
+    link["e2e_gbs"] = (h2d + d2h) * e2e_steps / e_max / 1e9
+    link["e2e_frac_of_concurrent"] = link["e2e_gbs"] / link["concurrent_gbs"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -637,7 +688,8 @@ def run_ours(args, world, rank, local):
         },
         "clocks": clk,
         "e2e": {"value": e_units / e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "method": e2e_method},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "method": e2e_method,
+                "host_link": link},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -71,6 +71,9 @@ def test_gpu_arm_line():
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert e2e["value"] != d["value"]
+    hl = e2e["host_link"]  # the step's copies alone, the ceiling e2e is judged against
+    assert hl["h2d_gbs"] > 0 and hl["d2h_gbs"] > 0 and hl["concurrent_gbs"] > 0
+    assert hl["e2e_frac_of_concurrent"] == pytest.approx(hl["e2e_gbs"] / hl["concurrent_gbs"])
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert d["gpu_launches"] == 5 * 20
     st = d["stages"]
