@@ -72,6 +72,11 @@ def test_random_expert_rows_and_unit_weights():
     (1024, 1024, 2, 16, 64, 2, 1),    # maximum ranks and Top-K
     (16, 4096, 20, 8, 16384, 16, 8),  # maximum experts and hidden size
     (64, 128, 3, 1, 32, 1, 1),        # K = 1, one channel
+    # notify's cluster kernel (more tokens than one CTA of a source rank holds):
+    (6, 24, 1500, 4, 64, 7, 2),       # P not a multiple of 4 (byte flag loads), clusters of 16
+    (8, 64, 1025, 8, 64, 300, 1),     # one token past the one-CTA limit (16 warps x 16 tokens x 4 steps)
+    (130, 260, 40, 8, 64, 50, 1),     # 33 rank groups: two rank blocks per warp; fewer tokens than channels
+    (64, 128, 1000, 4, 64, 1500, 1),  # 125 channel starts x 64 ranks per CTA, past the shared-memory buffer: written directly
 ])
 def test_edge_shapes(P, E, T, K, H, C, A):
     w = inputs.make(P, E, T, H, K, seed=P + K, mask_frac=0.05, C=C, expert_alignment=A)
