@@ -50,17 +50,19 @@ constexpr int kNotifyMaxCluster = 16;
 constexpr int kNotifyCache = 4;          // flag words a lane keeps in registers between the passes
 static_assert(kNotifyCache == 4, "the second pass selects among exactly four cached words");
 constexpr int kNotifyChanBuf = 4096;     // int32 entries of the channel-start buffer
+constexpr int kNotifySmemSteps = 16;     // steps per warp whose flags shared memory can keep
 
 struct NotifySmem {
-    size_t wcnt, xc, xr, tmp_r, base, total, rprev, ecnt, chv, bytes;
+    size_t wcnt, xc, xr, tmp_r, base, total, rprev, ecnt, chv, fsm, bytes;
 };
 
 // Shared memory (int32 unless noted): wcnt [warps][P]; xc, xr [cs][P] (the
 // cluster CTAs' totals and rank-prefix partials; this CTA's own row is the
 // one peers read); tmp_r [threads] int4; base [P];
 // total [P]; rprev [P]; ecnt [E/P]; chv [channels starting
-// in this CTA's tokens][P] when that fits kNotifyChanBuf.
-__host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs) {
+// in this CTA's tokens][P] when that fits kNotifyChanBuf; with fsteps > 0,
+// fsm uint32 [warps][fsteps][32]: each lane's flag words between the passes.
+__host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs, int fsteps) {
     NotifySmem m;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -77,6 +79,7 @@ __host__ __device__ inline NotifySmem notify_smem(int P, int E, int cs) {
     m.rprev = take(static_cast<size_t>(P) * 4);
     m.ecnt = take(static_cast<size_t>(E / P) * 4);
     m.chv = take(kNotifyChanBuf * 4);
+    m.fsm = take(static_cast<size_t>(kNotifyWarps) * fsteps * 32 * 4);
     m.bytes = o;
     return m;
 }
@@ -153,6 +156,7 @@ struct NotifyParams {
     const uint8_t* itr;
     int32_t *rpm, *cpm, *rcpm, *nrt, *nrtpe, *reo, *send_head;
     int64_t* part_row_base;
+    int32_t fsteps;     // kNotifySmemSteps when the flags are kept in shared memory, else 0
     uint64_t mq1, mq0;  // div_magic(cq + 1), div_magic(cq)
     // notify_small_kernel only: log2 of the lanes per token, rows of the two
     // partial-sum tables, division constants, shared-memory offsets (bytes)
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     const int cs = a.cs;
     const int r = static_cast<int>(cluster_ctarank());
     const int32_t s = static_cast<int32_t>(cluster_id_x());
-    const NotifySmem M = notify_smem(P, E, cs);
+    const NotifySmem M = notify_smem(P, E, cs, a.fsteps);
     int32_t* wcnt = reinterpret_cast<int32_t*>(smem + M.wcnt);
     int32_t* xc = reinterpret_cast<int32_t*>(smem + M.xc);
     int32_t* xr = reinterpret_cast<int32_t*>(smem + M.xr);
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
     int32_t* rprev = reinterpret_cast<int32_t*>(smem + M.rprev);
     int32_t* ecnt = reinterpret_cast<int32_t*>(smem + M.ecnt);
     int32_t* chv = reinterpret_cast<int32_t*>(smem + M.chv);
+    uint32_t* fsm = reinterpret_cast<uint32_t*>(smem + M.fsm);
     int32_t* ctot = xc + r * P;   // this CTA's totals (read by the peers)
     int32_t* rpart = xr + r * P;  // this CTA's rank-prefix partial (read by the peers)
 
@@ -241,9 +246,13 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
         for (int q = lane; q < P; q += 32) esum += __ldg(ecol + static_cast<int64_t>(q) * E + lb + warp);
     // --- 1. count ---------------------------------------------------------
     // With one block of rank groups and at most kNotifyCache steps per warp,
-    // a lane's flag words stay in registers for the second pass.
+    // a lane's flag words stay in registers for the second pass; with up to
+    // kNotifySmemSteps steps (a.fsteps > 0), in shared memory, all loaded at
+    // once.
     uint32_t fc[kNotifyCache];
     bool cached = false;
+    const bool scached = a.fsteps > 0;
+    uint32_t* fs = fsm + warp * (kNotifySmemSteps * 32) + lane;
     for (int rb = 0; rb * 32 < G; ++rb) {
         const int gn = min(32, G - rb * 32);
         int L = 1;
@@ -265,6 +274,18 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
                 c1 += byte_of(fc[i], 1);
                 c2 += byte_of(fc[i], 2);
                 c3 += byte_of(fc[i], 3);
+            }
+        } else if (scached) {
+#pragma unroll 8
+            for (int i = 0; i < kNotifySmemSteps; ++i) {
+                const int32_t t = sb + tk + i * tpw;
+                const uint32_t f =
+                    (g < gn && t < se) ? load_flags<A4>(src_rows + static_cast<int64_t>(t) * P, d, P) : 0u;
+                fs[i * 32] = f;
+                c0 += byte_of(f, 0);
+                c1 += byte_of(f, 1);
+                c2 += byte_of(f, 2);
+                c3 += byte_of(f, 3);
             }
         } else if (g < gn) {
 #pragma unroll 4
@@ -481,6 +502,10 @@ __global__ void __launch_bounds__(kNotifyThreads, 4) notify_kernel(const NotifyP
 #pragma unroll 1
         for (int32_t i = 0, t0 = sb; t0 < se; ++i, t0 += tpw) {
             const int k = i & (kNotifyCache - 1);
+            if (scached) {
+                step(t0 + tk, fs[i * 32]);
+                continue;
+            }
             if (!cached && k == 0) {
 #pragma unroll
                 for (int j = 0; j < kNotifyCache; ++j) {
@@ -792,8 +817,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) notify_small_kernel(const No
 struct NotifyPlan {
     bool small;  // one CTA per source rank (notify_small_kernel)
     int cluster;
+    int fsteps;  // cluster kernel: flags kept in shared memory (kNotifySmemSteps) or not (0)
     size_t smem;
 };
+
+// The cluster kernel keeps a lane's flags in shared memory between its passes
+// when one block of rank groups covers P, the register cache does not hold a
+// warp's steps and kNotifySmemSteps does.
+int notify_fsteps(const moe_shape& s, int cs) {
+    const int64_t T = s.S / s.P;
+    const int G = (s.P + 3) / 4;
+    if (G > 32) return 0;
+    int L = 1;
+    while (L < G) L <<= 1;
+    const int64_t tpw = 32 / L;
+    const int64_t seg = ceil_div(T, static_cast<int64_t>(cs) * kNotifyWarps);  // longest warp segment
+    const int64_t steps = ceil_div(seg, tpw);
+    return (steps > kNotifyCache && steps <= kNotifySmemSteps) ? kNotifySmemSteps : 0;
+}
 
 // One CTA of kSmallThreads covers a source rank when each of its 32 warps
 // needs at most kNotifyCache steps (the flags stay in registers) and the rank
@@ -832,7 +873,8 @@ NotifyPlan notify_plan(const moe_shape& s) {
     NotifyPlan p;
     p.small = false;
     p.cluster = c;
-    p.smem = notify_smem(s.P, s.E, c).bytes;
+    p.fsteps = notify_fsteps(s, c);
+    p.smem = notify_smem(s.P, s.E, c, p.fsteps).bytes;
     return p;
 }
 
@@ -909,7 +951,12 @@ cudaError_t launch_notify(const moe_shape& s, const int32_t* ntpr, const int32_t
     const int cs = cluster_size_for(fn, p.cluster, kNotifyThreads, p.smem);
     if (cs < 1) return cudaErrorInvalidConfiguration;
     auto kern = a4 ? notify_kernel<true> : notify_kernel<false>;
-    const size_t smem = notify_smem(s.P, s.E, cs).bytes;  // for the cluster size granted
+    a.fsteps = notify_fsteps(s, cs);
+    const size_t smem = notify_smem(s.P, s.E, cs, a.fsteps).bytes;  // for the cluster size granted
+    if (smem > p.smem) {  // a smaller cluster than planned may need the flag cache
+        e = prepare_kernel(fn, smem, kNotifyThreads, nullptr);
+        if (e != cudaSuccess) return e;
+    }
     a.cs = cs;
     a.lcs = 0;
     while ((1 << a.lcs) < cs) ++a.lcs;
