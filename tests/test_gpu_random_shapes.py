@@ -54,3 +54,39 @@ def test_random_shape_all_paths(P, E, T, H, K, quant, C, A, mask, routing, seed)
     if quant == 0 and P <= 64 and E <= 1024 and K <= 16 and P * C <= 4096:
         _check_fused(w)
     run_expert_major(w, quant=quant, y_mode="dequant" if quant else "identity")
+
+
+def _cluster_shapes(n=12, seed=4049):
+    """Longer source ranks (257-2000 tokens): layout in clusters of several
+    CTAs and notify's cluster kernel, with its flags kept in registers, kept in
+    shared memory or re-read, depending on P and T. Small H keeps the oracle
+    quick."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        P = int(rng.choice([2, 6, 8, 12, 24, 33, 48, 64, 65, 100, 128]))
+        T = int(rng.integers(257, max(258, min(2000, 40000 // P))))
+        E = P * int(rng.integers(1, 5))
+        K = int(rng.integers(1, min(16, E) + 1))
+        H = 8 * int(rng.integers(1, 33))
+        C = int(rng.integers(1, 3 * T // 2))
+        A = int(rng.choice([1, 1, 3]))
+        mask = float(rng.choice([0.0, 0.1]))
+        routing = "zipf" if rng.random() < 0.3 else "uniform"
+        out.append((P, E, T, H, K, C, A, mask, routing, 5000 + i))
+    return out
+
+
+CLUSTER_SHAPES = _cluster_shapes()
+
+
+@pytest.mark.parametrize("P,E,T,H,K,C,A,mask,routing,seed", CLUSTER_SHAPES,
+                         ids=[f"P{s[0]}E{s[1]}T{s[2]}H{s[3]}K{s[4]}C{s[5]}A{s[6]}" for s in CLUSTER_SHAPES])
+def test_random_long_ranks(P, E, T, H, K, C, A, mask, routing, seed):
+    w = inputs.make(P, E, T, H, K, routing=routing, mask_frac=mask, seed=seed, C=C, expert_alignment=A)
+    gpu = gp.run_gpu(w)
+    assert gpu["layout_err"] == 0 and gpu["dispatch_err"] == 0 and gpu["combine_err"] == 0
+    lay, nt = gp.oracle_tables(w)
+    gp.assert_tables_equal(gpu, lay, nt)
+    gp.compare_dispatch(w, 0, gpu, nt)
+    gp.compare_combine(w, gpu, nt)
