@@ -28,7 +28,7 @@
 //    shared memory, in CTA order, each CTA writing a share of the source
 //    rank's num_tokens_per_rank / num_tokens_per_expert row. No second pass
 //    over global memory and no cross-cluster synchronisation.
-//  * A source rank held by one CTA (T <= 256 tokens) skips the cluster
+//  * A source rank held by one CTA (T <= 512 tokens) skips the cluster
 //    exchange: its totals go straight from shared memory.
 //  * A one-block tail kernel folds the clusters' out-of-range flags into the
 //    caller's error word (only when an error word is given). It lets the next
@@ -48,7 +48,8 @@ constexpr bool kAtomicHist = false;
 constexpr bool kAtomicHist = true;
 #endif
 
-constexpr int kLayoutThreads = 256;
+constexpr int kLayoutThreads = 512;         // block size limit: one CTA holds up to 512 tokens
+constexpr int kLayoutClusterThreads = 256;  // block size of the CTAs of a cluster
 constexpr int kLayoutMaxCluster = 16;
 constexpr size_t kLayoutSmemBudget = 96 * 1024;
 
@@ -370,10 +371,17 @@ layout_err_kernel(int32_t P, const int32_t* __restrict__ bad_flags, int32_t* __r
 
 // CTAs per source rank (before the residency check of the cluster size) and
 // threads per CTA for a shape.
+// A source rank of up to kLayoutThreads tokens is one CTA (no cluster
+// exchange); a longer one is a cluster of CTAs of about
+// kLayoutClusterThreads tokens each. (Measured on GB300, layout + notify
+// inside a step: p128_e256_t512 30.0-32.0 us with one 512-thread CTA per
+// source rank against 33.2-33.4 us with two of 256; p8_e256_t4096 best with
+// 16 CTAs of 256, 13.8-15.1 us, against 8 of 512, 14.5-15.1 us.)
 void layout_geometry(const moe_shape& s, int* cs, int* threads) {
     const int64_t T = s.S / s.P;
-    int c = 1;  // a power of two, about kLayoutThreads tokens per CTA
-    while (c < kLayoutMaxCluster && static_cast<int64_t>(c) * kLayoutThreads < T) c <<= 1;
+    int c = 1;  // a power of two
+    if (T > kLayoutThreads)
+        while (c < kLayoutMaxCluster && static_cast<int64_t>(c) * kLayoutClusterThreads < T) c <<= 1;
     const int64_t n = ceil_div(T, c);
     int tb = static_cast<int>(round_up(n < 32 ? 32 : n, 32));
     if (tb > kLayoutThreads) tb = kLayoutThreads;
