@@ -10,8 +10,9 @@
 //   slot_row[g][k] = recv_expert_offset[e] + #(slots of expert e before (g, k))
 //   expert_part_base[d] = sum over d' < d of sum_l num_recv_tokens_per_expert[d'][l]
 //
-// Two launches over chunks of kChunk consecutive tokens, one CTA per chunk
-// and one thread per token (a token's K slots are contiguous in topk_idx):
+// Two launches over chunks of up to kChunk consecutive tokens (the plan's
+// power of two giving about 64 chunks), one CTA per chunk and one thread per
+// token (a token's K slots are contiguous in topk_idx):
 //  1. count: the chunk's expert histogram (shared-memory integer atomics)
 //     into scratch, expert-major: ecount[e][chunk];
 //  2. rows: each CTA adds, per expert, the counts of the chunks before its own

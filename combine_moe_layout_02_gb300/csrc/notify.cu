@@ -836,7 +836,7 @@ int notify_fsteps(const moe_shape& s, int cs) {
     return (steps > kNotifyCache && steps <= kNotifySmemSteps) ? kNotifySmemSteps : 0;
 }
 
-// One CTA of kSmallThreads covers a source rank when each of its 32 warps
+// One CTA of kSmallThreads covers a source rank when each of its kSmallWarps warps
 // needs at most kNotifyCache steps (the flags stay in registers) and the rank
 // groups fit one warp (P <= 128).
 bool notify_small(const moe_shape& s) {
